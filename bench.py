@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP32 matrix product C = A * B on GB300 (one JSON line).
+
+Default workload: M = N = K = 4096, A and B i.i.d. uniform[-1, 1) from seed 1
+(the pages' problem size, "GEMM from naive to tiled", section 二.1). A step
+is one call of the C ABI on device-resident inputs; L2 is flushed (a 256 MiB
+device memset) before every step, outside the timed events. Reported:
+
+  value      TFLOP/s = 2 M N K / mean device time of a step (CUDA events on
+             the launching stream), summed over ranks (replicas);
+  roofline   the FP32 FMA-pipe roofline: SMs x 128 FMA/clk x 2 flop x the
+             median SM clock sampled during the timed region ("alu" bound);
+  e2e        the same metric through sgemm_host(): pinned host A, B in,
+             host C out, copies inside the timed region;
+  cpu_baseline  the CPU oracle timed on this host's cores on a bounded row
+             sample of the same product.
+
+``--impl reference`` times the CPU oracle (the reference of this build) on
+the same workload instead. Under torchrun (N > 1) each rank runs its own
+replica on its own GPU; only rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FMA_PER_CLK_PER_SM = 128   # FP32 FMA lanes per SM (4 SMSPs x 32)
+L2_FLUSH_BYTES = 256 << 20
+CPU_SAMPLE_SECONDS = 12.0
+
+
+def flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def algorithmic_bytes(M, N, K):
+    return 4.0 * (M * K + K * N + M * N)
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp32_matrix_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel, workload):
+    """dram bytes per launch from the committed ncu record, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            recs = json.load(f)
+    except (OSError, ValueError):
+        return None
+    digest = source_digest()
+    for r in recs.get("records", []):
+        if (r.get("kernel") == kernel and r.get("workload") == workload
+                and r.get("source_sha256") == digest):
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev),
+                 "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0, "note": "nvidia-smi unavailable"}
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in self.lines:
+            p = [x.strip() for x in line.split(",")]
+            try:
+                sm.append(float(p[0]))
+                smax.append(float(p[1]))
+                power.append(float(p[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, p[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        # samples under load: the kernel keeps the SM clock up; idle samples at
+        # the edges of the window are dropped by taking the upper half.
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_rate(M, N, K, kind, seed, target_s=CPU_SAMPLE_SECONDS,
+                    min_rows=None):
+    """TFLOP/s of the CPU oracle on a row sample of the product, sized to run
+    about target_s seconds. Returns (tflops, rows, seconds, threads)."""
+    import numpy as np
+    import matgen
+    import oracle
+    threads = oracle.num_threads()
+    A = matgen.KINDS[kind](seed, matgen.MATRIX_A, M, K)
+    B = matgen.KINDS[kind](seed, matgen.MATRIX_B, K, N)
+    rows = max(threads, 1) if min_rows is None else min_rows
+    while True:
+        idx = np.arange(rows, dtype=np.int64) % M
+        t0 = time.perf_counter()
+        oracle.gemm_rows(A, B, idx)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 4 or rows >= M:
+            break
+        rows = min(M, rows * 2)
+    if dt < target_s and rows < M:
+        rows = int(min(M, max(rows, rows * target_s / max(dt, 1e-6))))
+        idx = np.arange(rows, dtype=np.int64) % M
+        t0 = time.perf_counter()
+        oracle.gemm_rows(A, B, idx)
+        dt = time.perf_counter() - t0
+    return flops(rows, N, K) / dt / 1e12, rows, dt, threads
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import matgen
+    import oracle
+    M, N, K = w["M"], w["N"], w["K"]
+    threads = oracle.num_threads()
+    A = matgen.KINDS[w["kind"]](w["seed"], matgen.MATRIX_A, M, K)
+    B = matgen.KINDS[w["kind"]](w["seed"], matgen.MATRIX_B, K, N)
+    # Size one step so that warmup + steps take about 90 s in total.
+    probe_rows = max(threads, 1)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, np.arange(probe_rows, dtype=np.int64))
+    t_row = (time.perf_counter() - t0) / probe_rows
+    budget = 90.0 / max(args.steps + args.warmup, 1)
+    rows = int(max(threads, min(M, budget / max(t_row, 1e-9))))
+    rows = max(1, min(M, rows))
+    times = []
+    for step in range(args.warmup + args.steps):
+        start = (step * rows) % M
+        idx = (start + np.arange(rows, dtype=np.int64)) % M
+        t0 = time.perf_counter()
+        oracle.gemm_rows(A, B, idx)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+    sec = sum(times) / len(times)
+    value = flops(rows, N, K) / sec / 1e12
+    sample = ("%d of %d rows of C per step (fp64 oracle, row order i-k-j)"
+              % (rows, M))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, extra={"sample": sample}),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = ("FP32 SGEMM TFLOP/s at M=N=K=4096 and % of GB300 FP32 FFMA peak "
+          "(1 GPU)")
+
+
+def config_of(w, extra=None):
+    c = {"workload": w["name"], "M": w["M"], "N": w["N"], "K": w["K"],
+         "layout": "row-major, dense leading dimensions",
+         "inputs": "%s, seed %d" % (w["kind"], w["seed"])}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_gpu(args, w):
+    import numpy as np
+    import torch
+    import matgen
+    import dense_fp32_matrix_gb300 as dfm
+    from dense_fp32_matrix_gb300 import build
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    build.build()
+
+    M, N, K = w["M"], w["N"], w["K"]
+    A = torch.from_numpy(matgen.KINDS[w["kind"]](w["seed"], 0, M, K)).cuda()
+    B = torch.from_numpy(matgen.KINDS[w["kind"]](w["seed"], 1, K, N)).cuda()
+    C = torch.empty((M, N), device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    path_name = args.path
+    plan = dfm.sgemm_plan(M, N, K, K, N, N, A.data_ptr(), B.data_ptr(),
+                          C.data_ptr()) if path_name == "auto" else path_name
+
+    def step():
+        dfm.sgemm_path(M, N, K, A, K, B, N, C, N, stream, path_name)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, site = dfm.sgemm_watchdog_status()
+    if st != 0:
+        raise RuntimeError("watchdog fired during warm-up (site %d)" % site)
+
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    st, site = dfm.sgemm_watchdog_status()
+    if st != 0:
+        raise RuntimeError("watchdog fired during timing (site %d)" % site)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    ms_step = sum(ms) / len(ms)
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tflops = flops(M, N, K) / (ms_step * 1e-3) / 1e12
+    value = tflops * world
+    clk = clocks.summary()
+
+    # e2e through the C ABI with host buffers: H2D inputs, compute, D2H C.
+    hA = A.cpu().pin_memory()
+    hB = B.cpu().pin_memory()
+    hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    dA = torch.empty_like(A)
+    dB = torch.empty_like(B)
+    dC = torch.empty_like(C)
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        dfm.sgemm_host(M, N, K, hA, K, hB, N, hC, N, dA, dB, dC, stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dfm.sgemm_host(M, N, K, hA, K, hB, N, hC, N, dA, dB, dC, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if not torch.equal(hC, C.cpu()):
+        raise RuntimeError("e2e result differs from the device-path result")
+
+    peak_clock_mhz = clk["sm_mhz"] or (clk["sm_max_mhz"] or None)
+    roof = None
+    if peak_clock_mhz:
+        peak = sms * FMA_PER_CLK_PER_SM * 2 * peak_clock_mhz * 1e6 / 1e12
+        kernel = {"tiled_tma": "k_tiled_tma", "tiled_ldg": "k_tiled_ldg"}.get(
+            plan, plan)
+        roof = {"bound": "alu", "achieved": tflops, "peak": peak,
+                "unit": "TFLOP/s", "frac": tflops / peak,
+                "traffic": recorded_traffic(kernel, w["name"]),
+                "kernel": kernel,
+                "peak_basis": ("%d SMs x %d FP32 FMA/clk x 2 flop x %.0f MHz "
+                               "(median SM clock sampled during the timed "
+                               "region)" % (sms, FMA_PER_CLK_PER_SM,
+                                            peak_clock_mhz))}
+        if clk["sm_max_mhz"]:
+            pmax = sms * FMA_PER_CLK_PER_SM * 2 * clk["sm_max_mhz"] * 1e6 / 1e12
+            roof["peak_at_max_clock"] = pmax
+            roof["frac_at_max_clock"] = tflops / pmax
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": config_of(w, extra={
+            "path": plan, "sms": sms, "gpu": props.name,
+            "l2": "flushed before every step (256 MiB device memset, "
+                  "outside the timed events)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}),
+        "roofline": roof,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
+                   "reasons": clk["reasons"], "samples": clk["samples"],
+                   "power_w_max": clk.get("power_w_max")},
+        "e2e": {"value": flops(M, N, K) / (e2e_ms * 1e-3) / 1e12 * world,
+                "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 4 * (M * K + K * N),
+                "d2h_bytes_per_step": 4 * M * N,
+                "api": "sgemm_host (pinned host buffers, 2-D async copies "
+                       "on the stream)"},
+        "gpu_launches": args.steps,
+        "ms_min": min(ms), "ms_median": statistics.median(ms),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows, sec, threads = cpu_oracle_rate(M, N, K, w["kind"],
+                                                   w["seed"])
+        line["cpu_baseline"] = {
+            "value": rate, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d of %d rows of C (fp64 oracle, %.1f s)" % (
+                rows, M, sec)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=None,
+                   help="workload name (default: the 4096^3 headline)")
+    p.add_argument("--path", default="auto",
+                   help="force a kernel path (auto, tiled_tma, tiled_ldg, ...)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    from matgen import workloads
+    w = workloads.by_name(args.workload) if args.workload else dict(
+        workloads.HEADLINE)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

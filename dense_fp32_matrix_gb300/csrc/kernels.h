@@ -1,0 +1,55 @@
+// Host-side launch interface between the C-ABI layer (sgemm_abi.cu) and the
+// translation units that hold the kernels. No torch types, plain pointers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dfm {
+
+struct GemmArgs {
+  int64_t M, N, K;
+  const float* A;
+  int64_t lda;
+  const float* B;
+  int64_t ldb;
+  float* C;
+  int64_t ldc;
+};
+
+// Tile geometry of the main kernel (also used by the host dispatcher).
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+constexpr int kTileK = 32;
+constexpr int kTileStages = 3;
+constexpr int kTileThreads = 256;
+
+// Dynamic shared memory of one tiled block, including alignment slack.
+size_t tiled_smem_bytes();
+
+// One-time per-device kernel attribute set-up. Returns a cudaError_t.
+cudaError_t tiled_init();
+cudaError_t small_init();
+
+// Main kernel with TMA loads. tmA / tmB must describe A (dims {K, M}, box
+// {kTileK, kTileM}, 128-byte swizzle) and B (dims {N, K}, box {kTileN,
+// kTileK}, no swizzle).
+cudaError_t launch_tiled_tma(const GemmArgs& g, const CUtensorMap& tmA,
+                             const CUtensorMap& tmB, int* status,
+                             cudaStream_t s);
+
+// Same tile core, operands fetched with predicated 4-byte cp.async (any
+// alignment, any leading dimension).
+cudaError_t launch_tiled_ldg(const GemmArgs& g, int* status, cudaStream_t s);
+
+// M == 1 and N == 1 bandwidth kernels; one-thread-per-output kernel.
+cudaError_t launch_gemv_row(const GemmArgs& g, int num_sms, cudaStream_t s);
+cudaError_t launch_gemv_col(const GemmArgs& g, int num_sms, cudaStream_t s);
+cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s);
+
+// One block waiting on an mbarrier that never completes (bounded).
+cudaError_t launch_watchdog_selftest(int* status, uint64_t limit_ns,
+                                     cudaStream_t s);
+
+}  // namespace dfm

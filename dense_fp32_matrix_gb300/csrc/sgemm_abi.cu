@@ -1,0 +1,344 @@
+// C ABI of the FP32 matrix-product library (declared in include/dfm_sgemm.h):
+// argument checks, the host-side path decision, one-time per-device set-up,
+// TMA descriptor encoding and the launches. The argument checks follow the
+// host wrappers of "GEMM from naive to tiled", section 十一.1 (device,
+// dtype, 2-D shape agreement), turned into status codes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/dfm_sgemm.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dfm {
+namespace {
+
+// Per-device status word of the bounded waits (see ptx.cuh).
+__device__ int g_status[4];
+
+constexpr int kMaxDevices = 64;
+// Largest M, N or K the int-indexed kernels accept (tile rounding included).
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1024;
+
+struct DeviceState {
+  std::once_flag once;
+  int err = SGEMM_OK;
+  int sms = 0;
+  int* status = nullptr;
+};
+
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
+                                   void*, const cuuint64_t*, const cuuint64_t*,
+                                   const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+void init_device(DeviceState& st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    st.err = SGEMM_ERR_CUDA;
+    return;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) !=
+          cudaSuccess) {
+    st.err = SGEMM_ERR_CUDA;
+    return;
+  }
+  if (major != 10 || minor != 3) {  // built for sm_103a only
+    st.err = SGEMM_ERR_UNSUPPORTED_DEVICE;
+    return;
+  }
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_status) !=
+          cudaSuccess ||
+      cudaMemset(st.status, 0, sizeof(int) * 4) != cudaSuccess ||
+      tiled_init() != cudaSuccess || small_init() != cudaSuccess) {
+    st.err = SGEMM_ERR_CUDA;
+    return;
+  }
+  st.err = SGEMM_OK;
+}
+
+// One-time set-up of the current device; returns its state or an error.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+  DeviceState& st = g_dev[dev];
+  std::call_once(st.once, [&] { init_device(st); });
+  *out = &st;
+  return st.err;
+}
+
+int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+               const void* B, int64_t ldb, const void* C, int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return SGEMM_ERR_INVALID_VALUE;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_TOO_LARGE;
+  if (M > 0 && N > 0) {
+    if (C == nullptr) return SGEMM_ERR_NULL_POINTER;
+    if (K > 0 && (A == nullptr || B == nullptr)) return SGEMM_ERR_NULL_POINTER;
+  }
+  return SGEMM_OK;
+}
+
+// Byte span [lo, hi) touched by a rows x cols matrix with leading dim ld.
+void span(uint64_t base, int64_t rows, int64_t cols, int64_t ld, uint64_t& lo,
+          uint64_t& hi) {
+  lo = base;
+  hi = base + uint64_t(((rows - 1) * ld + cols) * 4);
+}
+
+bool overlaps(uint64_t a, int64_t ar, int64_t ac, int64_t ald, uint64_t c,
+              int64_t cr, int64_t cc, int64_t cld) {
+  if (ar <= 0 || ac <= 0 || cr <= 0 || cc <= 0) return false;
+  uint64_t alo, ahi, clo, chi;
+  span(a, ar, ac, ald, alo, ahi);
+  span(c, cr, cc, cld, clo, chi);
+  return alo < chi && clo < ahi;
+}
+
+bool tma_operand_ok(uint64_t addr, int64_t ld) {
+  // TMA: 16-byte aligned base, row stride a multiple of 16 bytes and < 2^40.
+  return addr % 16 == 0 && (ld * 4) % 16 == 0 && ld * 4 < (int64_t(1) << 40);
+}
+
+// Host-only path choice (no device access).
+int plan_path(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              uint64_t a, uint64_t b) {
+  if (M == 0 || N == 0 || K == 0) return SGEMM_PATH_AUTO;  // no kernel
+  if (M == 1) return SGEMM_PATH_GEMV_ROW;
+  if (N == 1) return SGEMM_PATH_GEMV_COL;
+  if (tma_operand_ok(a, lda) && tma_operand_ok(b, ldb))
+    return SGEMM_PATH_TILED_TMA;
+  return SGEMM_PATH_TILED_LDG;
+}
+
+int encode_maps(const GemmArgs& g, CUtensorMap* tmA, CUtensorMap* tmB) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return SGEMM_ERR_CUDA;
+  // A: dims {K, M} (innermost first), row stride lda * 4 bytes, box
+  // {kTileK, kTileM} = 128 bytes x 128 rows, 128-byte swizzle.
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(g.K), cuuint64_t(g.M)};
+    const cuuint64_t strides[1] = {cuuint64_t(g.lda) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(kTileK), cuuint32_t(kTileM)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(g.A),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_CUDA;
+  }
+  // B: dims {N, K}, row stride ldb * 4 bytes, box {kTileN, kTileK} = 512
+  // bytes x 32 rows, no swizzle.
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(g.N), cuuint64_t(g.K)};
+    const cuuint64_t strides[1] = {cuuint64_t(g.ldb) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(kTileN), cuuint32_t(kTileK)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(g.B),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_CUDA;
+  }
+  return SGEMM_OK;
+}
+
+int to_status(cudaError_t e) {
+  if (e == cudaSuccess) return SGEMM_OK;
+  return (e == cudaErrorLaunchFailure || e == cudaErrorInvalidConfiguration ||
+          e == cudaErrorLaunchOutOfResources || e == cudaErrorInvalidValue)
+             ? SGEMM_ERR_LAUNCH
+             : SGEMM_ERR_CUDA;
+}
+
+int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+        const float* B, int64_t ldb, float* C, int64_t ldc, void* stream,
+        int path) {
+  int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (rc != SGEMM_OK) return rc;
+  if (path < 0 || path >= SGEMM_PATH_COUNT) return SGEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  const uint64_t a = reinterpret_cast<uint64_t>(A);
+  const uint64_t b = reinterpret_cast<uint64_t>(B);
+  const uint64_t c = reinterpret_cast<uint64_t>(C);
+  if (K > 0 && (overlaps(a, M, K, lda, c, M, N, ldc) ||
+                overlaps(b, K, N, ldb, c, M, N, ldc)))
+    return SGEMM_ERR_OVERLAP;
+
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != SGEMM_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (K == 0)  // empty sum
+    return to_status(cudaMemset2DAsync(C, size_t(ldc) * 4, 0, size_t(N) * 4,
+                                       size_t(M), s));
+
+  if (path == SGEMM_PATH_AUTO) path = plan_path(M, N, K, lda, ldb, a, b);
+  const GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc};
+  switch (path) {
+    case SGEMM_PATH_TILED_TMA: {
+      if (!tma_operand_ok(a, lda) || !tma_operand_ok(b, ldb))
+        return SGEMM_ERR_PATH;
+      CUtensorMap tmA, tmB;
+      rc = encode_maps(g, &tmA, &tmB);
+      if (rc != SGEMM_OK) return rc;
+      return to_status(launch_tiled_tma(g, tmA, tmB, st->status, s));
+    }
+    case SGEMM_PATH_TILED_LDG:
+      return to_status(launch_tiled_ldg(g, st->status, s));
+    case SGEMM_PATH_GEMV_ROW:
+      if (M != 1) return SGEMM_ERR_PATH;
+      return to_status(launch_gemv_row(g, st->sms, s));
+    case SGEMM_PATH_GEMV_COL:
+      if (N != 1) return SGEMM_ERR_PATH;
+      return to_status(launch_gemv_col(g, st->sms, s));
+    case SGEMM_PATH_NAIVE:
+      return to_status(launch_naive(g, s));
+    default:
+      return SGEMM_ERR_PATH;
+  }
+}
+
+}  // namespace
+}  // namespace dfm
+
+extern "C" {
+
+int sgemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+          const float* B, int64_t ldb, float* C, int64_t ldc, void* stream) {
+  return dfm::run(M, N, K, A, lda, B, ldb, C, ldc, stream, SGEMM_PATH_AUTO);
+}
+
+int sgemm_path(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+               const float* B, int64_t ldb, float* C, int64_t ldc,
+               void* stream, int path) {
+  return dfm::run(M, N, K, A, lda, B, ldb, C, ldc, stream, path);
+}
+
+int sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+               int64_t ldc, uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
+               int* path) {
+  if (path == nullptr) return SGEMM_ERR_NULL_POINTER;
+  // Pointer values stand in for the matrices: a zero address with elements
+  // to touch is a null-pointer error, as in sgemm.
+  const int rc = dfm::check_args(M, N, K, reinterpret_cast<const void*>(a_addr),
+                                 lda, reinterpret_cast<const void*>(b_addr),
+                                 ldb, reinterpret_cast<const void*>(c_addr), ldc);
+  if (rc != SGEMM_OK) return rc;
+  *path = dfm::plan_path(M, N, K, lda, ldb, a_addr, b_addr);
+  return SGEMM_OK;
+}
+
+int sgemm_host(int64_t M, int64_t N, int64_t K, const float* hA, int64_t lda,
+               const float* hB, int64_t ldb, float* hC, int64_t ldc,
+               float* dA, float* dB, float* dC, void* stream) {
+  int rc = dfm::check_args(M, N, K, hA, lda, hB, ldb, hC, ldc);
+  if (rc != SGEMM_OK) return rc;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  if (dC == nullptr || (K > 0 && (dA == nullptr || dB == nullptr)))
+    return SGEMM_ERR_NULL_POINTER;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K > 0) {
+    if (cudaMemcpy2DAsync(dA, size_t(K) * 4, hA, size_t(lda) * 4,
+                          size_t(K) * 4, size_t(M), cudaMemcpyHostToDevice,
+                          s) != cudaSuccess ||
+        cudaMemcpy2DAsync(dB, size_t(N) * 4, hB, size_t(ldb) * 4,
+                          size_t(N) * 4, size_t(K), cudaMemcpyHostToDevice,
+                          s) != cudaSuccess)
+      return SGEMM_ERR_CUDA;
+  }
+  rc = sgemm(M, N, K, dA, K > 0 ? K : 1, dB, N, dC, N, stream);
+  if (rc != SGEMM_OK) return rc;
+  if (cudaMemcpy2DAsync(hC, size_t(ldc) * 4, dC, size_t(N) * 4, size_t(N) * 4,
+                        size_t(M), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SGEMM_ERR_CUDA;
+  return SGEMM_OK;
+}
+
+int sgemm_watchdog_status(int* site) {
+  dfm::DeviceState* st = nullptr;
+  const int rc = dfm::device_state(&st);
+  if (rc != SGEMM_OK) return rc;
+  int word[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(word, st->status, sizeof(word), cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemset(st->status, 0, sizeof(word)) != cudaSuccess)
+    return SGEMM_ERR_CUDA;
+  if (word[0] == 0) return SGEMM_OK;
+  if (site != nullptr) *site = word[1];
+  return SGEMM_ERR_WATCHDOG;
+}
+
+int sgemm_watchdog_selftest(void* stream, int64_t timeout_ns) {
+  dfm::DeviceState* st = nullptr;
+  int rc = dfm::device_state(&st);
+  if (rc != SGEMM_OK) return rc;
+  if (timeout_ns < 1000000) timeout_ns = 1000000;
+  if (timeout_ns > 2000000000) timeout_ns = 2000000000;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dfm::launch_watchdog_selftest(st->status, uint64_t(timeout_ns), s) !=
+      cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SGEMM_ERR_CUDA;
+  return sgemm_watchdog_status(nullptr);
+}
+
+const char* sgemm_status_string(int status) {
+  switch (status) {
+    case SGEMM_OK: return "ok";
+    case SGEMM_ERR_INVALID_VALUE: return "invalid value";
+    case SGEMM_ERR_NULL_POINTER: return "null pointer";
+    case SGEMM_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+    case SGEMM_ERR_LAUNCH: return "kernel launch failed";
+    case SGEMM_ERR_WATCHDOG: return "device wait timed out";
+    case SGEMM_ERR_OVERLAP: return "C overlaps A or B";
+    case SGEMM_ERR_CUDA: return "CUDA runtime error";
+    case SGEMM_ERR_PATH: return "path cannot take these arguments";
+    case SGEMM_ERR_TOO_LARGE: return "size beyond the supported range";
+    default: return "unknown status";
+  }
+}
+
+const char* sgemm_path_name(int path) {
+  switch (path) {
+    case SGEMM_PATH_AUTO: return "auto";
+    case SGEMM_PATH_TILED_TMA: return "tiled_tma";
+    case SGEMM_PATH_TILED_LDG: return "tiled_ldg";
+    case SGEMM_PATH_GEMV_ROW: return "gemv_row";
+    case SGEMM_PATH_GEMV_COL: return "gemv_col";
+    case SGEMM_PATH_NAIVE: return "naive";
+    default: return "?";
+  }
+}
+
+int sgemm_version(void) { return 100; }
+
+}  // extern "C"

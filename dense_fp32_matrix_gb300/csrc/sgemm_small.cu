@@ -1,0 +1,230 @@
+// Bandwidth-bound and debug kernels of the FP32 matrix product.
+//
+//   * gemv_row (M == 1): c = a * B. Every element of B is used once, so the
+//     product is a stream over B ("GEMM from naive to tiled", section 十.2:
+//     arithmetic intensity 2 flops per 4 bytes of B). A block owns 16 output
+//     columns and all of K: 64 row groups of 4 lanes walk K with stride 64,
+//     each lane holding 4 columns (one 16-byte load per row when the layout
+//     allows), and a shared-memory reduction adds the 64 partial sums in a
+//     fixed order. No cross-block reduction, no workspace.
+//   * gemv_col (N == 1): c = A * b. One warp per row of A: coalesced
+//     (16-byte when aligned) reads along the row, a fixed shuffle tree at
+//     the end ("如何让计算受限问题真正达到计算受限", section 7, the GEMV case).
+//   * naive: one thread per output, K-loop from global memory, bounds
+//     checked ("GEMM from naive to tiled", section 三: thread x along N so a
+//     warp reads one contiguous row segment of B). A debug baseline only.
+//   * watchdog self-test: one block waits on an mbarrier nothing arrives at,
+//     through the same bounded wait the tiled kernel uses.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dfm {
+namespace {
+
+constexpr int ROW_COLS = 16;    // output columns per gemv_row block
+constexpr int ROW_GROUPS = 64;  // k-strided row groups per gemv_row block
+constexpr int ROW_THREADS = ROW_GROUPS * 4;
+constexpr int ROW_UNROLL = 8;
+
+template <bool VEC>
+__global__ void __launch_bounds__(ROW_THREADS)
+k_gemv_row(const float* __restrict__ a, const float* __restrict__ B,
+           long long ldb, float* __restrict__ c, int N, int K) {
+  __shared__ float part[ROW_GROUPS][ROW_COLS + 1];
+  const int tid = threadIdx.x;
+  const int grp = tid >> 2, q = tid & 3;
+  const int n = blockIdx.x * ROW_COLS + q * 4;  // first of this lane's 4 cols
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (VEC) {
+    // Caller guarantees ldb % 4 == 0, N % 4 == 0 and B 16-byte aligned, so
+    // a 4-column chunk is either fully inside [0, N) or fully outside.
+    if (n < N) {
+      const float* col = B + n;
+      int k = grp;
+      for (; k + (ROW_UNROLL - 1) * ROW_GROUPS < K; k += ROW_UNROLL * ROW_GROUPS) {
+        float4 v[ROW_UNROLL];
+        float s[ROW_UNROLL];
+#pragma unroll
+        for (int u = 0; u < ROW_UNROLL; ++u) {
+          v[u] = __ldg(reinterpret_cast<const float4*>(
+              col + (long long)(k + u * ROW_GROUPS) * ldb));
+          s[u] = __ldg(a + k + u * ROW_GROUPS);
+        }
+#pragma unroll
+        for (int u = 0; u < ROW_UNROLL; ++u) {
+          acc[0] = fmaf(s[u], v[u].x, acc[0]);
+          acc[1] = fmaf(s[u], v[u].y, acc[1]);
+          acc[2] = fmaf(s[u], v[u].z, acc[2]);
+          acc[3] = fmaf(s[u], v[u].w, acc[3]);
+        }
+      }
+      for (; k < K; k += ROW_GROUPS) {
+        const float4 v =
+            __ldg(reinterpret_cast<const float4*>(col + (long long)k * ldb));
+        const float s = __ldg(a + k);
+        acc[0] = fmaf(s, v.x, acc[0]);
+        acc[1] = fmaf(s, v.y, acc[1]);
+        acc[2] = fmaf(s, v.z, acc[2]);
+        acc[3] = fmaf(s, v.w, acc[3]);
+      }
+    }
+  } else {
+    // Any layout: the 4 lanes of a group read 16 consecutive columns, lane
+    // q columns n0 + q + 4 e, one float each, predicated on N.
+    const int n0 = blockIdx.x * ROW_COLS;
+    for (int k = grp; k < K; k += ROW_GROUPS) {
+      const float s = __ldg(a + k);
+      const float* row = B + (long long)k * ldb + n0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = q + 4 * e;
+        if (n0 + j < N) acc[e] = fmaf(s, __ldg(row + j), acc[e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) part[grp][VEC ? q * 4 + e : q + 4 * e] = acc[e];
+  __syncthreads();
+  if (tid < ROW_COLS) {
+    const int j = blockIdx.x * ROW_COLS + tid;
+    float s = 0.f;
+    for (int g = 0; g < ROW_GROUPS; ++g) s += part[g][tid];
+    if (j < N) c[j] = s;
+  }
+}
+
+constexpr int COL_WARPS = 8;
+
+template <bool VEC>
+__global__ void __launch_bounds__(COL_WARPS * 32)
+k_gemv_col(const float* __restrict__ A, long long lda,
+           const float* __restrict__ b, long long ldb, float* __restrict__ c,
+           long long ldc, int M, int K) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = blockIdx.x * COL_WARPS + warp; i < M;
+       i += gridDim.x * COL_WARPS) {
+    const float* row = A + (long long)i * lda;
+    float acc = 0.f;
+    if (VEC) {
+      // Caller guarantees lda % 4 == 0, ldb == 1, A and b 16-byte aligned.
+      const int K4 = K >> 2;
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      const float4* b4 = reinterpret_cast<const float4*>(b);
+      int k = lane;
+      for (; k + 96 < K4; k += 128) {
+        float4 x[4], y[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          x[u] = __ldg(r4 + k + 32 * u);
+          y[u] = __ldg(b4 + k + 32 * u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc = fmaf(x[u].x, y[u].x, acc);
+          acc = fmaf(x[u].y, y[u].y, acc);
+          acc = fmaf(x[u].z, y[u].z, acc);
+          acc = fmaf(x[u].w, y[u].w, acc);
+        }
+      }
+      for (; k < K4; k += 32) {
+        const float4 x = __ldg(r4 + k), y = __ldg(b4 + k);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+        acc = fmaf(x.z, y.z, acc);
+        acc = fmaf(x.w, y.w, acc);
+      }
+      for (int kk = 4 * K4 + lane; kk < K; kk += 32)
+        acc = fmaf(__ldg(row + kk), __ldg(b + kk), acc);
+    } else {
+      for (int k = lane; k < K; k += 32)
+        acc = fmaf(__ldg(row + k), __ldg(b + (long long)k * ldb), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) c[(long long)i * ldc] = acc;
+  }
+}
+
+__global__ void k_naive(const float* __restrict__ A, long long lda,
+                        const float* __restrict__ B, long long ldb,
+                        float* __restrict__ C, long long ldc, int M, int N,
+                        int K) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  for (int i = blockIdx.y * blockDim.y + threadIdx.y; i < M;
+       i += gridDim.y * blockDim.y) {
+    if (j >= N) continue;
+    float acc = 0.f;
+    for (int k = 0; k < K; ++k)
+      acc = fmaf(A[(long long)i * lda + k], B[(long long)k * ldb + j], acc);
+    C[(long long)i * ldc + j] = acc;
+  }
+}
+
+__global__ void k_watchdog_selftest(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // Nothing arrives on this barrier: the wait must end by its limit.
+  const bool ok = mbar_wait_bounded(b, 0, threadIdx.x == 0 ? status : nullptr,
+                                    kSiteSelftest, limit_ns);
+  __syncthreads_or(!ok);
+}
+
+}  // namespace
+
+cudaError_t small_init() { return cudaSuccess; }
+
+cudaError_t launch_gemv_row(const GemmArgs& g, int num_sms, cudaStream_t s) {
+  (void)num_sms;
+  // 16-byte loads need aligned rows and whole 4-column chunks (N % 4 == 0),
+  // so no load reaches past column N - 1.
+  const bool vec = (g.ldb % 4 == 0) && (g.N % 4 == 0) &&
+                   (reinterpret_cast<uintptr_t>(g.B) % 16 == 0);
+  const unsigned blocks = unsigned((g.N + ROW_COLS - 1) / ROW_COLS);
+  if (vec)
+    k_gemv_row<true><<<blocks, ROW_THREADS, 0, s>>>(g.A, g.B, g.ldb, g.C,
+                                                     int(g.N), int(g.K));
+  else
+    k_gemv_row<false><<<blocks, ROW_THREADS, 0, s>>>(g.A, g.B, g.ldb, g.C,
+                                                      int(g.N), int(g.K));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_col(const GemmArgs& g, int num_sms, cudaStream_t s) {
+  const bool vec = (g.lda % 4 == 0) && (g.ldb == 1) &&
+                   (reinterpret_cast<uintptr_t>(g.A) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(g.B) % 16 == 0);
+  long long blocks = (g.M + COL_WARPS - 1) / COL_WARPS;
+  const long long cap = (long long)num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  if (vec)
+    k_gemv_col<true><<<unsigned(blocks), COL_WARPS * 32, 0, s>>>(
+        g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M), int(g.K));
+  else
+    k_gemv_col<false><<<unsigned(blocks), COL_WARPS * 32, 0, s>>>(
+        g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M), int(g.K));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s) {
+  const dim3 block(32, 8);
+  long long gy = (g.M + 7) / 8;
+  if (gy > 65535) gy = 65535;
+  const dim3 grid(unsigned((g.N + 31) / 32), unsigned(gy));
+  k_naive<<<grid, block, 0, s>>>(g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M),
+                                 int(g.N), int(g.K));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_watchdog_selftest(int* status, uint64_t limit_ns,
+                                     cudaStream_t s) {
+  k_watchdog_selftest<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace dfm

@@ -1,0 +1,158 @@
+/*
+ * dfm_sgemm.h -- C ABI of the GB300 (sm_103a) FP32 matrix-product library.
+ *
+ * The operation (all entry points that compute):
+ *
+ *     C[i*ldc + j] = sum_{k=0}^{K-1} A[i*lda + k] * B[k*ldb + j]
+ *                    for 0 <= i < M, 0 <= j < N
+ *
+ * with A (M x K), B (K x N) and C (M x N) row-major fp32 with leading
+ * dimensions lda, ldb, ldc in elements. Definitions followed:
+ *   - "CUDA 算子优化：GEMM" (llm-tech.com.cn/posts/cuda-gemm), section
+ *     "矩阵乘法": C_ij = sum_k A_ik B_kj, A M x K, B K x N, 2MNK flops.
+ *   - "GEMM from naive to tiled" (arganzheng.life), section 二.1: FP32,
+ *     row-major, C = A * B; section 三.1: kernels take const float*
+ *     __restrict__ A, B and write float* C; section 七: shapes that are not
+ *     multiples of the tile are handled by zero-filled loads and predicated
+ *     stores.
+ *   - hotelren.com/news/4711315 (inner vs outer product GEMM), section 4.2:
+ *     the leading dimension is passed separately from the logical width.
+ *
+ * Semantics shared by every computing entry point:
+ *   - C is overwritten (alpha = 1, beta = 0). Elements of C outside
+ *     i < M, j < N (the pitch padding ldc > N) are never written. A and B
+ *     are only read inside their logical extent (never in the padding).
+ *   - Summation is in fp32 with fused multiply-add, k in an implementation
+ *     order; results are deterministic run to run for a given shape, layout
+ *     and path. On integer-valued inputs whose partial sums stay below 2^24
+ *     in magnitude the result is exact.
+ *   - M == 0 or N == 0: nothing is done. K == 0: C[0:M, 0:N] is set to 0.
+ *   - NaN / Inf inputs propagate as IEEE fp32 arithmetic gives them.
+ *
+ * Memory and streams:
+ *   - A, B, C are device pointers of the calling thread's current CUDA
+ *     device, owned by the caller. Alignment is never an error: pointers or
+ *     leading dimensions that rule out 16-byte vector / TMA access select a
+ *     slower path of the same result class.
+ *   - C must not overlap A or B (SGEMM_ERR_OVERLAP).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Every call is asynchronous on that stream; the library never
+ *     synchronises. Errors found on the host are returned before anything is
+ *     enqueued.
+ *   - No entry point allocates device memory per call. The first call on a
+ *     device does one-time set-up (device query, kernel attributes, the
+ *     address of the per-device status word); make that first call outside
+ *     any stream capture.
+ *
+ * Status codes: 0 on success, a negative SGEMM_ERR_* value otherwise;
+ * sgemm_status_string() names each.
+ */
+#ifndef DFM_SGEMM_H
+#define DFM_SGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SGEMM_OK 0
+#define SGEMM_ERR_INVALID_VALUE (-1)    /* negative size or ld below width  */
+#define SGEMM_ERR_NULL_POINTER (-2)     /* null pointer with elements to use */
+#define SGEMM_ERR_UNSUPPORTED_DEVICE (-3) /* current device is not sm_103  */
+#define SGEMM_ERR_LAUNCH (-4)           /* kernel launch failed            */
+#define SGEMM_ERR_WATCHDOG (-5)         /* a bounded device wait timed out  */
+#define SGEMM_ERR_OVERLAP (-6)          /* C overlaps A or B               */
+#define SGEMM_ERR_CUDA (-7)             /* another CUDA runtime error      */
+#define SGEMM_ERR_PATH (-8)             /* forced path cannot take the call */
+#define SGEMM_ERR_TOO_LARGE (-9)        /* size beyond a path's limit      */
+
+/* Kernel paths (sgemm_path / sgemm_plan). */
+#define SGEMM_PATH_AUTO 0
+#define SGEMM_PATH_TILED_TMA 1  /* TMA-fed multistage tile kernel (aligned) */
+#define SGEMM_PATH_TILED_LDG 2  /* same tile core, 4-byte async loads     */
+#define SGEMM_PATH_GEMV_ROW 3   /* M == 1: c = a * B, column blocks       */
+#define SGEMM_PATH_GEMV_COL 4   /* N == 1: c = A * b, one warp per row     */
+#define SGEMM_PATH_NAIVE 5      /* one thread per output (debug baseline)  */
+#define SGEMM_PATH_COUNT 6
+
+/*
+ * sgemm: C = A * B as described above, on `stream`.
+ * Arguments: M, N, K >= 0; lda >= max(1, K); ldb >= max(1, N);
+ * ldc >= max(1, N). Pointers may be NULL only when the matrix has no
+ * elements to read or write.
+ * Errors: SGEMM_ERR_INVALID_VALUE, SGEMM_ERR_NULL_POINTER,
+ * SGEMM_ERR_OVERLAP, SGEMM_ERR_UNSUPPORTED_DEVICE, SGEMM_ERR_CUDA,
+ * SGEMM_ERR_LAUNCH. Watchdog timeouts are reported afterwards by
+ * sgemm_watchdog_status().
+ */
+int sgemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+          const float* B, int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/*
+ * sgemm_path: as sgemm, but runs the kernel path `path` (SGEMM_PATH_*)
+ * instead of the one sgemm would choose. Returns SGEMM_ERR_PATH when that
+ * path cannot take the arguments (e.g. TILED_TMA with an ld that is not a
+ * multiple of 4, GEMV_ROW with M != 1). Meant for tests and measurement.
+ */
+int sgemm_path(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+               const float* B, int64_t ldb, float* C, int64_t ldc,
+               void* stream, int path);
+
+/*
+ * sgemm_plan: the path sgemm would take for these arguments, decided on the
+ * host only (no device is touched). a_addr / b_addr / c_addr are the pointer
+ * values (only their alignment is used). Writes the SGEMM_PATH_* value to
+ * *path. Returns the same argument errors as sgemm (no device errors).
+ */
+int sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+               int64_t ldc, uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
+               int* path);
+
+/*
+ * sgemm_host: C = A * B for HOST matrices hA (ld lda), hB (ld ldb), hC
+ * (ld ldc). The caller provides device staging buffers dA (M*K floats),
+ * dB (K*N floats) and dC (M*N floats), dense (ld = K, N, N). On `stream`:
+ * copy hA -> dA and hB -> dB, run sgemm on the staging buffers, copy
+ * dC -> hC. Asynchronous: hC is valid after the stream is synchronised; host
+ * buffers should be pinned for the copies to overlap. Same errors as sgemm.
+ */
+int sgemm_host(int64_t M, int64_t N, int64_t K, const float* hA, int64_t lda,
+               const float* hB, int64_t ldb, float* hC, int64_t ldc,
+               float* dA, float* dB, float* dC, void* stream);
+
+/*
+ * sgemm_watchdog_status: every wait inside the kernels (on an mbarrier or a
+ * peer block's flag) is bounded; on timeout the kernel records the failure
+ * in a per-device status word, abandons its tile and exits without trapping.
+ * This call reads and clears that word for the current device. Call it after
+ * synchronising the streams that ran sgemm. Returns SGEMM_OK or
+ * SGEMM_ERR_WATCHDOG (then *site, if not NULL, receives the wait-site id),
+ * or SGEMM_ERR_CUDA.
+ */
+int sgemm_watchdog_status(int* site);
+
+/*
+ * sgemm_watchdog_selftest: launches one block that waits on an mbarrier
+ * nothing ever arrives at, with the same bounded-wait code the kernels use
+ * and a limit of `timeout_ns` (clamped to [1e6, 2e9] ns). Synchronises the
+ * stream and returns what sgemm_watchdog_status then reports (expected:
+ * SGEMM_ERR_WATCHDOG). Used to test failure detection without a GPU fault.
+ */
+int sgemm_watchdog_selftest(void* stream, int64_t timeout_ns);
+
+/* Human-readable name of a status code (static storage). */
+const char* sgemm_status_string(int status);
+
+/* Name of an SGEMM_PATH_* value (static storage), "?" when unknown. */
+const char* sgemm_path_name(int path);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFM_SGEMM_H */

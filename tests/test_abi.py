@@ -1,0 +1,115 @@
+"""The C-ABI library: builds, loads, exports every declared symbol, and its
+host-only logic (argument checks, path planning). No device is touched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_fp32_matrix_gb300 as dfm
+from dense_fp32_matrix_gb300 import _native, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dfm_sgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _native.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sgemm\w*)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("sgemm", "sgemm_path", "sgemm_plan", "sgemm_host",
+              "sgemm_watchdog_status", "sgemm_watchdog_selftest",
+              "sgemm_status_string", "sgemm_path_name", "sgemm_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(_native.exported_symbols())
+
+
+def test_exports_are_plain_c(lib):
+    # extern "C": the unmangled names resolve through dlsym.
+    handle = ctypes.CDLL(_native.LIB_PATH)
+    for name in declared_functions():
+        assert getattr(handle, name) is not None
+
+
+def test_version_and_strings(lib):
+    assert dfm.sgemm_version() >= 100
+    for name, code in dfm.STATUS.items():
+        s = dfm.sgemm_status_string(code)
+        assert s and s != "unknown status", name
+    for name, code in dfm.PATHS.items():
+        assert dfm.sgemm_path_name(code) == name
+    assert dfm.sgemm_path_name(99) == "?"
+
+
+A16 = 0x7f0000000000       # 256-byte aligned fake addresses (never used)
+B16 = 0x7f0010000000
+C16 = 0x7f0020000000
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,a,b,expect", [
+    (4096, 4096, 4096, 4096, 4096, 4096, A16, B16, "tiled_tma"),
+    (256, 256, 256, 256, 256, 256, A16, B16, "tiled_tma"),
+    (4095, 4097, 1023, 1023, 4097, 4097, A16, B16, "tiled_ldg"),  # ld % 4
+    (127, 129, 33, 33, 129, 129, A16, B16, "tiled_ldg"),
+    (4096, 4096, 4096, 4096, 4096, 4096, A16 + 4, B16, "tiled_ldg"),  # align
+    (4096, 4096, 4096, 4100, 4096, 4096, A16, B16, "tiled_tma"),  # pitch
+    (1, 4096, 4096, 4096, 4096, 4096, A16, B16, "gemv_row"),
+    (4096, 1, 4096, 4096, 1, 1, A16, B16, "gemv_col"),
+    (1, 1, 7, 7, 1, 1, A16, B16, "gemv_row"),
+    (5, 5, 0, 1, 5, 5, 0, 0, "auto"),      # K = 0: memset, no kernel
+    (0, 5, 3, 3, 5, 5, 0, 0, "auto"),      # empty output
+])
+def test_plan(lib, M, N, K, lda, ldb, ldc, a, b, expect):
+    assert dfm.sgemm_plan(M, N, K, lda, ldb, ldc, a, b, C16) == expect
+
+
+@pytest.mark.parametrize("args,code", [
+    ((-1, 4, 4, 4, 4, 4), "SGEMM_ERR_INVALID_VALUE"),
+    ((4, 4, 4, 3, 4, 4), "SGEMM_ERR_INVALID_VALUE"),   # lda < K
+    ((4, 4, 4, 4, 3, 4), "SGEMM_ERR_INVALID_VALUE"),   # ldb < N
+    ((4, 4, 4, 4, 4, 3), "SGEMM_ERR_INVALID_VALUE"),   # ldc < N
+    ((4, 4, 4, 4, 4, 0), "SGEMM_ERR_INVALID_VALUE"),
+    ((1 << 31, 4, 4, 4, 4, 4), "SGEMM_ERR_TOO_LARGE"),
+])
+def test_plan_argument_errors(lib, args, code):
+    with pytest.raises(dfm.SgemmError) as e:
+        dfm.sgemm_plan(*args, A16, B16, C16)
+    assert e.value.status == dfm.STATUS[code]
+
+
+def test_plan_null_pointers(lib):
+    with pytest.raises(dfm.SgemmError) as e:
+        dfm.sgemm_plan(4, 4, 4, 4, 4, 4, 0, B16, C16)
+    assert e.value.status == dfm.STATUS["SGEMM_ERR_NULL_POINTER"]
+    with pytest.raises(dfm.SgemmError) as e:
+        dfm.sgemm_plan(4, 4, 4, 4, 4, 4, A16, B16, 0)
+    assert e.value.status == dfm.STATUS["SGEMM_ERR_NULL_POINTER"]
+    # nothing to read: null A and B are fine when K == 0
+    assert dfm.sgemm_plan(4, 4, 0, 1, 4, 4, 0, 0, C16) == "auto"
+
+
+def test_sgemm_rejects_bad_arguments_before_touching_a_device(lib):
+    # Argument errors are returned before any CUDA call, so this runs on a
+    # host without a GPU.
+    L = _native.lib()
+    assert L.sgemm(-1, 4, 4, A16, 4, B16, 4, C16, 4, None) == -1
+    assert L.sgemm(4, 4, 4, A16, 2, B16, 4, C16, 4, None) == -1
+    assert L.sgemm(4, 4, 4, None, 4, B16, 4, C16, 4, None) == -2
+    assert L.sgemm_path(4, 4, 4, A16, 4, B16, 4, C16, 4, None, 42) == -1
+    # M == 0: nothing to do, no device needed
+    assert L.sgemm(0, 4, 4, None, 4, None, 4, None, 4, None) == 0
