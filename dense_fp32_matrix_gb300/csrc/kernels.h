@@ -28,15 +28,29 @@ constexpr int kTileThreads = 256;
 // Dynamic shared memory of one tiled block, including alignment slack.
 size_t tiled_smem_bytes();
 
-// One-time per-device kernel attribute set-up. Returns a cudaError_t.
-cudaError_t tiled_init();
+// One-time per-device kernel attribute set-up. Returns a cudaError_t;
+// tiled_init also reports how many TMA tile blocks fit on one SM.
+cudaError_t tiled_init(int* tma_blocks_per_sm);
 cudaError_t small_init();
+
+// Stream-K schedule of the TMA tile kernel: G = min(resident blocks, T)
+// persistent blocks share T = tiles x iters_per_tile k-slice iterations.
+struct SkPlan {
+  int64_t tiles = 0;
+  int64_t iters_per_tile = 0;
+  int64_t total_iters = 0;
+  int grid = 0;
+  size_t ws_floats = 0;   // workspace: 2 partial tiles per block
+};
+SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K, int resident_blocks);
 
 // Main kernel with TMA loads. tmA / tmB must describe A (dims {K, M}, box
 // {kTileK, kTileM}, 128-byte swizzle) and B (dims {N, K}, box {kTileN,
-// kTileK}, no swizzle).
+// kTileK}, no swizzle). ws holds pl.ws_floats floats; counters holds
+// pl.tiles ints, all zero (the kernel leaves them zero when it completes).
 cudaError_t launch_tiled_tma(const GemmArgs& g, const CUtensorMap& tmA,
-                             const CUtensorMap& tmB, int* status,
+                             const CUtensorMap& tmB, const SkPlan& pl,
+                             float* ws, int* counters, int* status,
                              cudaStream_t s);
 
 // Same tile core, operands fetched with predicated 4-byte cp.async (any

@@ -26,7 +26,14 @@ struct DeviceState {
   std::once_flag once;
   int err = SGEMM_OK;
   int sms = 0;
+  int tma_blocks_per_sm = 0;
   int* status = nullptr;
+  // Stream-K workspace of the TMA path: partial tiles, then tile counters.
+  std::mutex ws_mu;
+  float* ws = nullptr;
+  size_t ws_floats = 0;
+  int* counters = nullptr;
+  size_t counters_len = 0;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -75,7 +82,8 @@ void init_device(DeviceState& st) {
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_status) !=
           cudaSuccess ||
       cudaMemset(st.status, 0, sizeof(int) * 4) != cudaSuccess ||
-      tiled_init() != cudaSuccess || small_init() != cudaSuccess) {
+      tiled_init(&st.tma_blocks_per_sm) != cudaSuccess ||
+      st.tma_blocks_per_sm < 1 || small_init() != cudaSuccess) {
     st.err = SGEMM_ERR_CUDA;
     return;
   }
@@ -91,6 +99,31 @@ int device_state(DeviceState** out) {
   std::call_once(st.once, [&] { init_device(st); });
   *out = &st;
   return st.err;
+}
+
+// Make the device's stream-K workspace at least `floats` partial-tile
+// floats and `tiles` counters. Growing frees the old buffers (cudaFree waits
+// for the device) and zeroes the new counters.
+int ensure_workspace(DeviceState& st, size_t floats, size_t tiles) {
+  std::lock_guard<std::mutex> lock(st.ws_mu);
+  if (floats > st.ws_floats) {
+    if (st.ws != nullptr) cudaFree(st.ws);
+    st.ws = nullptr;
+    st.ws_floats = 0;
+    if (cudaMalloc(&st.ws, floats * sizeof(float)) != cudaSuccess)
+      return SGEMM_ERR_CUDA;
+    st.ws_floats = floats;
+  }
+  if (tiles > st.counters_len) {
+    if (st.counters != nullptr) cudaFree(st.counters);
+    st.counters = nullptr;
+    st.counters_len = 0;
+    if (cudaMalloc(&st.counters, tiles * sizeof(int)) != cudaSuccess ||
+        cudaMemset(st.counters, 0, tiles * sizeof(int)) != cudaSuccess)
+      return SGEMM_ERR_CUDA;
+    st.counters_len = tiles;
+  }
+  return SGEMM_OK;
 }
 
 int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
@@ -133,7 +166,11 @@ int plan_path(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
   if (M == 0 || N == 0 || K == 0) return SGEMM_PATH_AUTO;  // no kernel
   if (M == 1) return SGEMM_PATH_GEMV_ROW;
   if (N == 1) return SGEMM_PATH_GEMV_COL;
-  if (tma_operand_ok(a, lda) && tma_operand_ok(b, ldb))
+  // The stream-K schedule counts k-slice iterations in 32 bits.
+  const int64_t iters = ((M + kTileM - 1) / kTileM) *
+                        ((N + kTileN - 1) / kTileN) *
+                        ((K + kTileK - 1) / kTileK);
+  if (tma_operand_ok(a, lda) && tma_operand_ok(b, ldb) && iters < (1ll << 31))
     return SGEMM_PATH_TILED_TMA;
   return SGEMM_PATH_TILED_LDG;
 }
@@ -207,10 +244,17 @@ int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
     case SGEMM_PATH_TILED_TMA: {
       if (!tma_operand_ok(a, lda) || !tma_operand_ok(b, ldb))
         return SGEMM_ERR_PATH;
+      if (plan_stream_k(M, N, K, 1).total_iters >= (1ll << 31))
+        return SGEMM_ERR_TOO_LARGE;
       CUtensorMap tmA, tmB;
       rc = encode_maps(g, &tmA, &tmB);
       if (rc != SGEMM_OK) return rc;
-      return to_status(launch_tiled_tma(g, tmA, tmB, st->status, s));
+      const SkPlan pl =
+          plan_stream_k(M, N, K, st->sms * st->tma_blocks_per_sm);
+      rc = ensure_workspace(*st, pl.ws_floats, size_t(pl.tiles));
+      if (rc != SGEMM_OK) return rc;
+      return to_status(launch_tiled_tma(g, tmA, tmB, pl, st->ws,
+                                        st->counters, st->status, s));
     }
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
@@ -294,6 +338,15 @@ int sgemm_watchdog_status(int* site) {
     return SGEMM_ERR_CUDA;
   if (word[0] == 0) return SGEMM_OK;
   if (site != nullptr) *site = word[1];
+  // A block that abandoned its range may have left stream-K tile counters
+  // raised; clear them so later calls start from zero.
+  {
+    std::lock_guard<std::mutex> lock(st->ws_mu);
+    if (st->counters != nullptr &&
+        cudaMemset(st->counters, 0, st->counters_len * sizeof(int)) !=
+            cudaSuccess)
+      return SGEMM_ERR_CUDA;
+  }
   return SGEMM_ERR_WATCHDOG;
 }
 

@@ -159,24 +159,143 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 }
 
 // ------------------------------------------------------------ TMA kernel
+//
+// Persistent stream-K schedule ("GEMM from naive to tiled", section 十.1:
+// split the total multiply-add work, tiles x k-slices, evenly over a fixed
+// set of resident blocks instead of dealing whole tiles in waves, so no
+// partly filled last wave is left; section 八.2 measures that loss). Block c
+// of G owns k-slice iterations [c T / G, (c+1) T / G) of the T = tiles x I
+// iterations laid out tile by tile (I = k-slices per tile, tiles in grouped
+// raster order). Its range is a run of segments, each a k-range of one tile:
+// a segment that covers its whole tile is stored directly; a partial one
+// writes its fp32 partial tile to the workspace and bumps the tile's
+// counter. The block that brings the counter to (pieces - 1) adds all pieces
+// in piece order (k order), stores C and resets the counter. Nobody waits on
+// another block, so there is no co-residency requirement; the summation order
+// is fixed, so results are deterministic for a given shape and grid size.
+
+struct SkParams {
+  int M, N, K;
+  long long ldc;
+  int tiles_m, tiles_n;
+  int iters_per_tile;      // I
+  int total_iters;         // T = tiles * I (< 2^31, checked by the host)
+  int grid;                // G, with G <= T
+  float* ws;               // 2 G partial tiles of BM x BN floats
+  int* counters;           // one per tile, zero between calls
+  int vec_store;
+  int* status;
+};
+
+__device__ __forceinline__ int range_begin(int c, const SkParams& p) {
+  return int((long long)c * p.total_iters / p.grid);
+}
+
+// Index of the block whose range holds iteration x: the largest c with
+// floor(c T / G) <= x.
+__device__ __forceinline__ int block_of(int x, const SkParams& p) {
+  return int(((long long)(x + 1) * p.grid + p.total_iters - 1) /
+             p.total_iters) - 1;
+}
+
+// Partial tiles are stored thread-major: value q of thread t at q * NT + t,
+// so the stores and loads of a block are fully coalesced 8-byte accesses.
+__device__ __forceinline__ void store_partial(const f2 (&acc)[TM][4],
+                                              unsigned long long* w) {
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) __stcg(w + (i * 4 + j) * NT + threadIdx.x, acc[i][j].v);
+}
+
+__device__ __forceinline__ void add_partial(f2 (&sum)[TM][4],
+                                            const unsigned long long* w) {
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const unsigned long long v = __ldcg(w + (i * 4 + j) * NT + threadIdx.x);
+      asm("add.rn.f32x2 %0, %0, %1;" : "+l"(sum[i][j].v) : "l"(v));
+    }
+}
+
+// Finish one partial segment of `tile` held in acc. my_slot: workspace slot
+// of this piece. Every piece, the last one included, goes through the
+// workspace, so the block that arrives last re-reads all pieces in piece
+// order and the sum does not depend on which block that is.
+__device__ __forceinline__ void sk_fixup(const f2 (&acc)[TM][4], int tile,
+                                         int my_slot, const SkParams& p,
+                                         float* C, int m0, int n0, int r0,
+                                         int c0, int* s_flag) {
+  unsigned long long* ws = reinterpret_cast<unsigned long long*>(p.ws);
+  constexpr int SLOT = BM * BN / 2;  // f2 values per partial tile
+  store_partial(acc, ws + (long long)my_slot * SLOT);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *s_flag = atomicAdd(&p.counters[tile], 1);
+  __syncthreads();
+  const int x0 = tile * p.iters_per_tile;
+  const int c_first = block_of(x0, p);
+  const int c_last = block_of(x0 + p.iters_per_tile - 1, p);
+  const int pieces = c_last - c_first + 1;
+  const int arrived = *s_flag;
+  __syncthreads();  // s_flag is reused by the next segment
+  if (arrived != pieces - 1) return;
+  __threadfence();
+  f2 sum[TM][4];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sum[i][j].v = 0ull;
+  for (int j = 0; j < pieces; ++j) {
+    const int cj = c_first + j;
+    // A block's piece of this tile is its first segment when its range
+    // starts inside the tile, else the last segment of its range.
+    const int slot = 2 * cj + (range_begin(cj, p) >= x0 ? 0 : 1);
+    add_partial(sum, ws + (long long)slot * SLOT);
+  }
+  store_tile(sum, C, p.M, p.N, p.ldc, m0, n0, r0, c0, p.vec_store != 0);
+  if (threadIdx.x == 0) p.counters[tile] = 0;
+}
+
+// Producer state of the TMA loads, kept in shared memory: only thread 0
+// touches it, so it costs the 255 other threads no registers.
+struct Producer {
+  int kt, tile, m0, n0;
+};
 
 __global__ void __launch_bounds__(NT, 2)
 k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
             const __grid_constant__ CUtensorMap tmB, float* __restrict__ C,
-            int M, int N, int K, long long ldc, int vec_store, int* status) {
+            const SkParams p) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_flag;
+  __shared__ Producer s_prod;
   uint8_t* smem = aligned_smem(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
   const uint32_t bar0 = smem_u32(sB + STAGES * B_STAGE);
-  const Geometry g = block_geometry(M, N, K);
   const int tid = threadIdx.x;
+  const int I = p.iters_per_tile;
+  const int it_begin = range_begin(blockIdx.x, p);
+  const int it_end = range_begin(blockIdx.x + 1, p);
 
-  auto issue = [&](int tile, int slot) {
+  // Issue the loads of the next iteration into `slot` and advance.
+  auto issue_next = [&](int slot) {
+    Producer q = s_prod;
     const uint32_t bar = bar0 + 8 * slot;
     mbar_arrive_expect_tx(bar, STAGE_TX);
-    tma_load_2d(smem_u32(sA + slot * A_STAGE), &tmA, tile * BK, g.m0, bar);
-    tma_load_2d(smem_u32(sB + slot * B_STAGE), &tmB, g.n0, tile * BK, bar);
+    tma_load_2d(smem_u32(sA + slot * A_STAGE), &tmA, q.kt * BK, q.m0, bar);
+    tma_load_2d(smem_u32(sB + slot * B_STAGE), &tmB, q.n0, q.kt * BK, bar);
+    if (++q.kt == I) {
+      q.kt = 0;
+      ++q.tile;
+      int pm, pn;
+      tile_coords(q.tile, p.tiles_m, p.tiles_n, pm, pn);
+      q.m0 = pm * BM;
+      q.n0 = pn * BN;
+    }
+    s_prod = q;
   };
 
   if (tid == 0) {
@@ -184,10 +303,18 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
     tma_prefetch_desc(&tmB);
     for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
     mbar_fence_init();
+    Producer q;
+    q.tile = it_begin / I;
+    q.kt = it_begin - q.tile * I;
+    int pm, pn;
+    tile_coords(q.tile, p.tiles_m, p.tiles_n, pm, pn);
+    q.m0 = pm * BM;
+    q.n0 = pn * BN;
+    s_prod = q;
+    for (int s = 0; s < STAGES - 1 && it_begin + s < it_end; ++s)
+      issue_next(s);
   }
   __syncthreads();
-  if (tid == 0)
-    for (int s = 0; s < STAGES - 1 && s < g.T; ++s) issue(s, s);
 
   f2 acc[TM][4];
 #pragma unroll
@@ -195,36 +322,61 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j].v = 0ull;
 
-  const uint8_t* a_rows = sA + g.r0 * A_ROW;
-  const uint8_t* b_cols = sB + g.c0 * 4;
+  const int lane_m = (tid & 31) >> 2;
+  const uint8_t* a_rows = sA + ((tid >> 5) / WARPS_N * WM + lane_m) * A_ROW;
+  const uint8_t* b_cols =
+      sB + ((tid >> 5) % WARPS_N * WN + (tid & 3) * 4) * 4;
   int slot = 0;
   uint32_t phase = 0;
-  for (int t = 0; t < g.T; ++t) {
-    const bool ok = mbar_wait_bounded(bar0 + 8 * slot, phase, status,
+  int tile_end = (it_begin / I + 1) * I;  // end of the current tile's slices
+  for (int it = it_begin; it < it_end; ++it) {
+    const bool ok = mbar_wait_bounded(bar0 + 8 * slot, phase, p.status,
                                       kSiteTiledFull, kWaitLimitNs);
     // Uniform abort decision; also the barrier after which the slot read in
-    // step t-1 is free for the refill below.
+    // the previous iteration is free for the refill below.
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         // Let this block's own copies still in flight settle (bounded).
-        for (int u = t; u < g.T && u < t + STAGES - 1; ++u) {
-          const int su = u % STAGES;
-          mbar_wait_bounded(bar0 + 8 * su, (u / STAGES) & 1, nullptr,
-                            kSiteTiledDrain, kWaitLimitNs / 100);
+        int su = slot;
+        uint32_t ph = phase;
+        for (int u = it; u < it_end && u < it + STAGES - 1; ++u) {
+          mbar_wait_bounded(bar0 + 8 * su, ph, nullptr, kSiteTiledDrain,
+                            kWaitLimitNs / 100);
+          if (++su == STAGES) { su = 0; ph ^= 1u; }
         }
       }
       return;
     }
-    const int nt = t + STAGES - 1;
-    if (tid == 0 && nt < g.T) issue(nt, nt % STAGES);
+    if (tid == 0 && it + STAGES - 1 < it_end)
+      issue_next(slot == 0 ? STAGES - 1 : slot - 1);
     compute_slice(acc, a_rows + slot * A_STAGE, b_cols + slot * B_STAGE,
-                  g.lane_m);
+                  lane_m);
     if (++slot == STAGES) {
       slot = 0;
       phase ^= 1u;
     }
+    if (it + 1 == it_end || it + 1 == tile_end) {
+      // End of a segment: [max(it_begin, tile start), it] of one tile.
+      const int tile = tile_end / I - 1;
+      const int tile_begin = tile_end - I;
+      int pm, pn;
+      tile_coords(tile, p.tiles_m, p.tiles_n, pm, pn);
+      const int warp = tid >> 5;
+      const int r0 = warp / WARPS_N * WM + lane_m;
+      const int c0 = warp % WARPS_N * WN + (tid & 3) * 4;
+      if (it_begin <= tile_begin && it + 1 == tile_end)
+        store_tile(acc, C, p.M, p.N, p.ldc, pm * BM, pn * BN, r0, c0,
+                   p.vec_store != 0);
+      else
+        sk_fixup(acc, tile, 2 * blockIdx.x + (it_begin >= tile_begin ? 0 : 1),
+                 p, C, pm * BM, pn * BN, r0, c0, &s_flag);
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j].v = 0ull;
+      tile_end += I;
+    }
   }
-  store_tile(acc, C, M, N, ldc, g.m0, g.n0, g.r0, g.c0, vec_store != 0);
 }
 
 // ------------------------------------------------------- cp.async kernel
@@ -309,22 +461,50 @@ bool vec_ok(const GemmArgs& g) {
 
 size_t tiled_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t tiled_init() {
+cudaError_t tiled_init(int* tma_blocks_per_sm) {
   cudaError_t e = cudaFuncSetAttribute(
       k_tiled_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
       int(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_tiled_ldg,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(SMEM_BYTES));
+  e = cudaFuncSetAttribute(k_tiled_ldg,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      tma_blocks_per_sm, k_tiled_tma, NT, SMEM_BYTES);
+}
+
+SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K, int resident_blocks) {
+  SkPlan pl;
+  pl.tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  pl.iters_per_tile = (K + BK - 1) / BK;
+  pl.total_iters = pl.tiles * pl.iters_per_tile;
+  pl.grid = resident_blocks < pl.total_iters ? resident_blocks
+                                             : int(pl.total_iters);
+  if (pl.grid < 1) pl.grid = 1;
+  pl.ws_floats = size_t(2) * pl.grid * BM * BN;
+  return pl;
 }
 
 cudaError_t launch_tiled_tma(const GemmArgs& g, const CUtensorMap& tmA,
-                             const CUtensorMap& tmB, int* status,
+                             const CUtensorMap& tmB, const SkPlan& pl,
+                             float* ws, int* counters, int* status,
                              cudaStream_t s) {
-  k_tiled_tma<<<grid_tiles(g), NT, SMEM_BYTES, s>>>(
-      tmA, tmB, g.C, int(g.M), int(g.N), int(g.K), (long long)g.ldc,
-      vec_ok(g) ? 1 : 0, status);
+  SkParams p;
+  p.M = int(g.M);
+  p.N = int(g.N);
+  p.K = int(g.K);
+  p.ldc = (long long)g.ldc;
+  p.tiles_m = int((g.M + BM - 1) / BM);
+  p.tiles_n = int((g.N + BN - 1) / BN);
+  p.iters_per_tile = int(pl.iters_per_tile);
+  p.total_iters = int(pl.total_iters);
+  p.grid = pl.grid;
+  p.ws = ws;
+  p.counters = counters;
+  p.vec_store = vec_ok(g) ? 1 : 0;
+  p.status = status;
+  k_tiled_tma<<<pl.grid, NT, SMEM_BYTES, s>>>(tmA, tmB, g.C, p);
   return cudaGetLastError();
 }
 
