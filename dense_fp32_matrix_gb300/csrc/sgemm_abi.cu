@@ -8,7 +8,7 @@
 
 #include <mutex>
 
-#include "../../include/dfm_sgemm.h"
+#include "dfm_sgemm.h"
 #include "kernels.h"
 #include "ptx.cuh"
 

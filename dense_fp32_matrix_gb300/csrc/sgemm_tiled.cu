@@ -39,9 +39,14 @@ namespace {
 
 constexpr int BM = kTileM, BN = kTileN, BK = kTileK, STAGES = kTileStages;
 constexpr int NT = kTileThreads;
-constexpr int WM = 64, WN = 32;       // warp tile
+constexpr int TM = 8;                 // rows per lane
+constexpr int LANES_N = 4;            // lanes of a warp along N
+constexpr int LANES_M = 32 / LANES_N; // lanes along M (a lane's rows are
+                                      // LANES_M apart)
+constexpr int WM = LANES_M * TM;      // warp tile 64 x 32
+constexpr int WN = LANES_N * 8;
 constexpr int WARPS_N = BN / WN;      // 4 (2 along M)
-constexpr int TM = 8;                 // rows per lane, 8 apart
+constexpr int COL_SPLIT = 4 * LANES_N;  // a lane's 2nd 4-column chunk offset
 constexpr int A_ROW = BK * 4;         // bytes per A row in shared memory
 constexpr int B_ROW = BN * 4;         // bytes per B row in shared memory
 constexpr int A_STAGE = BM * A_ROW;   // 16 KiB
@@ -52,7 +57,8 @@ constexpr size_t SMEM_BYTES = size_t(STAGES) * STAGE_TX + 64 + 1024;
 
 static_assert(A_ROW == 128, "A rows are one 128-byte swizzle span");
 static_assert((BM / WM) * (BN / WN) * 32 == NT, "warp grid");
-static_assert(WM == 8 * TM && WN == 4 * 8, "lane grid 8 x 4, lane tile 8 x 8");
+static_assert(LANES_M * LANES_N == 32 && LANES_M <= 8 && 8 % LANES_M == 0,
+              "lane grid");
 
 // Tile id -> (tile row, tile col) in groups of GROUP_M tile rows, column by
 // column inside a group, so blocks running together share A and B slices in
@@ -70,9 +76,9 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n,
 }
 
 // One BK-deep k-slice of rank-1 updates from shared memory.
-// a_rows: this lane's first A row in the stage; b_cols: this lane's first B
-// column in row 0 of the stage; lane_m == (row mod 8) for all of the lane's
-// rows.
+// a_rows: this lane's first A row in the stage (row r0; its rows are
+// r0 + LANES_M i); b_cols: this lane's first B column in row 0 of the stage;
+// lane_m: r0 mod LANES_M (r0 - lane_m is a multiple of 8).
 __device__ __forceinline__ void compute_slice(f2 (&acc)[TM][4],
                                               const uint8_t* a_rows,
                                               const uint8_t* b_cols,
@@ -80,15 +86,18 @@ __device__ __forceinline__ void compute_slice(f2 (&acc)[TM][4],
 #pragma unroll
   for (int kq = 0; kq < BK / 4; ++kq) {
     float4 a[TM];
-    const int chunk = (kq ^ lane_m) << 4;
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
-      a[i] = *reinterpret_cast<const float4*>(a_rows + i * 8 * A_ROW + chunk);
+    for (int i = 0; i < TM; ++i) {
+      const int chunk = (kq ^ ((lane_m + LANES_M * i) & 7)) << 4;
+      a[i] = *reinterpret_cast<const float4*>(a_rows + i * LANES_M * A_ROW +
+                                              chunk);
+    }
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint8_t* brow = b_cols + (kq * 4 + kk) * B_ROW;
       const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(brow);
-      const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(brow + 64);
+      const ulonglong2 b1 =
+          *reinterpret_cast<const ulonglong2*>(brow + 4 * COL_SPLIT);
       const f2 bp0{b0.x}, bp1{b0.y}, bp2{b1.x}, bp3{b1.y};
 #pragma unroll
       for (int i = 0; i < TM; ++i) {
@@ -104,19 +113,19 @@ __device__ __forceinline__ void compute_slice(f2 (&acc)[TM][4],
   }
 }
 
-// Write the lane's 8 x 8 results. Row i of the lane is m0 + r0 + 8 i; its
-// columns are n0 + c0 + {0..3} and n0 + c0 + 16 + {0..3}.
+// Write the lane's 8 x 8 results. Row i of the lane is m0 + r0 + LANES_M i;
+// its columns are n0 + c0 + {0..3} and n0 + c0 + COL_SPLIT + {0..3}.
 __device__ __forceinline__ void store_tile(const f2 (&acc)[TM][4], float* C,
                                            int M, int N, long long ldc, int m0,
                                            int n0, int r0, int c0, bool vec) {
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
-    const int r = m0 + r0 + 8 * i;
+    const int r = m0 + r0 + LANES_M * i;
     if (r >= M) continue;
     float* crow = C + (long long)r * ldc;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int c = n0 + c0 + 16 * h;
+      const int c = n0 + c0 + COL_SPLIT * h;
       if (vec && c + 3 < N) {
         ulonglong2 v;
         v.x = acc[i][2 * h].v;
@@ -146,9 +155,9 @@ __device__ __forceinline__ Geometry block_geometry(int M, int N, int K) {
   g.m0 = pm * BM;
   g.n0 = pn * BN;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  g.lane_m = lane >> 2;
+  g.lane_m = lane / LANES_N;
   g.r0 = (warp / WARPS_N) * WM + g.lane_m;
-  g.c0 = (warp % WARPS_N) * WN + (lane & 3) * 4;
+  g.c0 = (warp % WARPS_N) * WN + (lane % LANES_N) * 4;
   g.T = (K + BK - 1) / BK;
   return g;
 }
@@ -322,10 +331,10 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j].v = 0ull;
 
-  const int lane_m = (tid & 31) >> 2;
+  const int lane_m = (tid & 31) / LANES_N;
   const uint8_t* a_rows = sA + ((tid >> 5) / WARPS_N * WM + lane_m) * A_ROW;
   const uint8_t* b_cols =
-      sB + ((tid >> 5) % WARPS_N * WN + (tid & 3) * 4) * 4;
+      sB + ((tid >> 5) % WARPS_N * WN + (tid % LANES_N) * 4) * 4;
   int slot = 0;
   uint32_t phase = 0;
   int tile_end = (it_begin / I + 1) * I;  // end of the current tile's slices
@@ -363,7 +372,7 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
       tile_coords(tile, p.tiles_m, p.tiles_n, pm, pn);
       const int warp = tid >> 5;
       const int r0 = warp / WARPS_N * WM + lane_m;
-      const int c0 = warp % WARPS_N * WN + (tid & 3) * 4;
+      const int c0 = warp % WARPS_N * WN + (tid % LANES_N) * 4;
       if (it_begin <= tile_begin && it + 1 == tile_end)
         store_tile(acc, C, p.M, p.N, p.ldc, pm * BM, pn * BN, r0, c0,
                    p.vec_store != 0);
