@@ -13,6 +13,7 @@ from . import _native
 
 __all__ = [
     "SgemmError", "sgemm", "sgemm_path", "sgemm_plan", "sgemm_host",
+    "sgemm_noalloc",
     "sgemm_watchdog_status", "sgemm_watchdog_selftest",
     "sgemm_status_string", "sgemm_path_name", "sgemm_version", "matmul",
     "PATHS", "STATUS",
@@ -75,6 +76,13 @@ def sgemm_path(M, N, K, A, lda, B, ldb, C, ldc, stream=None, path="auto"):
     _check(_native.lib().sgemm_path(M, N, K, _ptr(A), lda, _ptr(B), ldb,
                                     _ptr(C), ldc, _stream(stream),
                                     _path(path)), "sgemm_path")
+
+
+def sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> None:
+    """As ``sgemm`` but never allocates device memory (fixed scratch)."""
+    _check(_native.lib().sgemm_noalloc(M, N, K, _ptr(A), lda, _ptr(B), ldb,
+                                       _ptr(C), ldc, _stream(stream)),
+           "sgemm_noalloc")
 
 
 def sgemm_plan(M, N, K, lda, ldb, ldc, a_addr, b_addr, c_addr) -> str:

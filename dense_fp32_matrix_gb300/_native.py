@@ -28,6 +28,8 @@ _SIGNATURES = {
     "sgemm_plan": ([_i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_uint64,
                     ctypes.c_uint64, ctypes.c_uint64, ctypes.POINTER(_int)],
                    _int),
+    "sgemm_noalloc": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp],
+                      _int),
     "sgemm_host": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp,
                     _vp, _vp, _vp], _int),
     "sgemm_watchdog_status": ([ctypes.POINTER(_int)], _int),

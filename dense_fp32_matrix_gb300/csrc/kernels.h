@@ -67,3 +67,17 @@ cudaError_t launch_watchdog_selftest(int* status, uint64_t limit_ns,
                                      cudaStream_t s);
 
 }  // namespace dfm
+
+namespace dfm {
+
+// C = A * B like sgemm, but the stream-K TMA path takes its partial tiles
+// and tile counters from caller-provided device scratch (ws: ws_floats
+// floats, counters: counters_len ints) with at most grid_cap blocks, and no
+// device memory is allocated. The counters used are cleared on the stream
+// before the launch. Returns an SGEMM_* status.
+int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
+                     int64_t lda, const float* B, int64_t ldb, float* C,
+                     int64_t ldc, void* stream, float* ws, size_t ws_floats,
+                     int* counters, size_t counters_len, int grid_cap);
+
+}  // namespace dfm

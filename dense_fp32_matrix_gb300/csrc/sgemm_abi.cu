@@ -272,6 +272,56 @@ int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
 }
 
 }  // namespace
+
+int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
+                     int64_t lda, const float* B, int64_t ldb, float* C,
+                     int64_t ldc, void* stream, float* ws, size_t ws_floats,
+                     int* counters, size_t counters_len, int grid_cap) {
+  int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (rc != SGEMM_OK) return rc;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  const uint64_t a = reinterpret_cast<uint64_t>(A);
+  const uint64_t b = reinterpret_cast<uint64_t>(B);
+  const uint64_t c = reinterpret_cast<uint64_t>(C);
+  if (K > 0 && (overlaps(a, M, K, lda, c, M, N, ldc) ||
+                overlaps(b, K, N, ldb, c, M, N, ldc)))
+    return SGEMM_ERR_OVERLAP;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != SGEMM_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0)
+    return to_status(cudaMemset2DAsync(C, size_t(ldc) * 4, 0, size_t(N) * 4,
+                                       size_t(M), s));
+  const int path = plan_path(M, N, K, lda, ldb, a, b);
+  const GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc};
+  switch (path) {
+    case SGEMM_PATH_TILED_TMA: {
+      CUtensorMap tmA, tmB;
+      rc = encode_maps(g, &tmA, &tmB);
+      if (rc != SGEMM_OK) return rc;
+      int resident = st->sms * st->tma_blocks_per_sm;
+      if (resident > grid_cap) resident = grid_cap;
+      const SkPlan pl = plan_stream_k(M, N, K, resident);
+      if (pl.ws_floats > ws_floats || size_t(pl.tiles) > counters_len)
+        return SGEMM_ERR_TOO_LARGE;
+      rc = to_status(
+          cudaMemsetAsync(counters, 0, size_t(pl.tiles) * sizeof(int), s));
+      if (rc != SGEMM_OK) return rc;
+      return to_status(
+          launch_tiled_tma(g, tmA, tmB, pl, ws, counters, st->status, s));
+    }
+    case SGEMM_PATH_TILED_LDG:
+      return to_status(launch_tiled_ldg(g, st->status, s));
+    case SGEMM_PATH_GEMV_ROW:
+      return to_status(launch_gemv_row(g, st->sms, s));
+    case SGEMM_PATH_GEMV_COL:
+      return to_status(launch_gemv_col(g, st->sms, s));
+    default:
+      return SGEMM_ERR_PATH;
+  }
+}
+
 }  // namespace dfm
 
 extern "C" {

@@ -123,6 +123,37 @@ int sgemm_host(int64_t M, int64_t N, int64_t K, const float* hA, int64_t lda,
                float* dA, float* dB, float* dC, void* stream);
 
 /*
+ * sgemm_noalloc: C = A * B with the semantics, arguments and errors of
+ * sgemm, for callers that must not allocate device memory at the point of
+ * use -- code whose device memory is all owned by another allocator (a
+ * framework's caching pool, a fixed budget), latency-critical loops that
+ * cannot afford the device-wide synchronisation cudaMalloc/cudaFree imply,
+ * or plug-ins in hosts that forbid allocation after start-up. sgemm() may
+ * grow its workspace with cudaMalloc; this entry point never calls
+ * cudaMalloc, cudaFree or any allocating routine. The pages have no
+ * counterpart of this entry point.
+ *
+ * Scratch: the stream-K partial tiles and tile counters of the TMA path live
+ * in one fixed device array of 20 MiB + 64 KiB that every device which loads
+ * the library holds until the process exits. Limits: at most 16384 output
+ * tiles of 128 x 128 (e.g. M = N = 16384); larger M x N returns
+ * SGEMM_ERR_TOO_LARGE before any work is enqueued. The stream-K grid is
+ * capped at 160 blocks.
+ *
+ * The first call on a device fetches the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call shares the array: calls whose
+ * kernels may overlap on the GPU (unordered streams) race and must be
+ * ordered by the caller. Each call clears the counters it uses on `stream`
+ * before its kernel runs. Results may differ from sgemm() in the last bits
+ * (a different stream-K split changes the fp32 summation order); both are
+ * deterministic and exact on small-integer inputs.
+ */
+int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float* A,
+                  int64_t lda, const float* B, int64_t ldb, float* C,
+                  int64_t ldc, void* stream);
+
+/*
  * sgemm_watchdog_status: every wait inside the kernels (on an mbarrier or a
  * peer block's flag) is bounded; on timeout the kernel records the failure
  * in a per-device status word, abandons its tile and exits without trapping.
