@@ -19,11 +19,19 @@ struct GemmArgs {
 };
 
 // Tile geometry of the main kernel (also used by the host dispatcher).
+// Block tile kTileM x kTileN, k-slices of kTileK, a kTileStages-deep ring;
+// kTileThreads threads, kTileMinBlocks resident blocks per SM; each lane
+// owns kLaneRows rows x (4 * kLaneChunks) columns of the block tile, with
+// kLanesN lanes of a warp along N.
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
 constexpr int kTileK = 32;
 constexpr int kTileStages = 3;
 constexpr int kTileThreads = 256;
+constexpr int kTileMinBlocks = 2;
+constexpr int kLaneRows = 8;
+constexpr int kLaneChunks = 2;
+constexpr int kLanesN = 4;
 
 // Dynamic shared memory of one tiled block, including alignment slack.
 size_t tiled_smem_bytes();

@@ -2,28 +2,27 @@
 //
 // Structure (prior art: "GEMM from naive to tiled", sections 五-七, and
 // "SGEMM 纯 CUDA 优化总结", ex8/ex9 and Q3-Q8; redesigned for GB300):
-//   * output-stationary: one block owns a 128 x 128 tile of C and walks all
-//     of K ("如何让计算受限问题真正达到计算受限", section 1.2);
-//   * BK = 32 k-slices staged through a 3-deep shared-memory ring, so BK is
-//     decoupled from BM/BN (ex8) and each k-slice costs one block barrier
-//     (ex9 / section 六);
-//   * 8 warps in a 2 x 4 grid, each owning a 64 x 32 warp tile; lanes in an
-//     8 x 4 grid (Q8: a square-ish lane shape shares both operands), each
-//     lane an 8 x 8 register tile updated by rank-1 (outer-product) steps
-//     acc[i][j] += a[i] * b[j] (section 五.1; hotelren.com section 2.2);
-//   * the FMA is the Blackwell packed form fma.rn.f32x2, two independent
-//     IEEE fp32 fused multiply-adds per instruction, which halves the issue
-//     slots the 64 FMAs of one k-step need and leaves room for the shared
-//     loads; every output element still receives exactly one fp32 FMA per k,
-//     k ascending;
+//   * output-stationary: a block owns a BM x BN tile of C and accumulates
+//     over K in registers ("如何让计算受限问题真正达到计算受限", section 1.2);
+//   * BK = 32 k-slices staged through a STAGES-deep shared-memory ring, so
+//     BK is decoupled from BM/BN (ex8) and each k-slice costs one block
+//     barrier (ex9 / section 六);
+//   * warps tile the block; each lane owns TM rows x 4 TNC columns and
+//     updates them by rank-1 (outer-product) steps acc[i][j] += a[i] * b[j]
+//     (section 五.1; hotelren.com section 2.2);
+//   * the FMA is the Blackwell packed form fma.rn.f32x2: two independent
+//     IEEE fp32 fused multiply-adds per instruction on adjacent output
+//     columns, with the row operand a[i] used for both halves; it halves the
+//     issue slots the FMAs need. Every output element still receives exactly
+//     one fp32 FMA per k, k ascending within a block's k-range;
 //   * A stays K-major in shared memory (a TMA box cannot transpose, section
-//     六.3): the lane reads 4 consecutive k of each of its 8 rows with one
-//     128-bit load; rows of a lane are 8 apart so the 8 lanes of a load hit 8
-//     consecutive rows, and the TMA 128-byte swizzle (16-byte chunk c of row
-//     r stored at chunk c ^ (r mod 8), the XOR swizzle of Q7) makes those
-//     8 x 16 bytes land in 32 distinct banks;
-//   * B is N-major; a lane's 8 columns are two 4-column chunks 16 apart, so
-//     the 4 distinct lane columns of a load cover 64 contiguous bytes
+//     六.3): a lane reads 4 consecutive k of each of its TM rows with one
+//     128-bit load. A lane's rows are LANES_M apart, so the lanes of one load
+//     hit consecutive rows, and the TMA 128-byte swizzle (16-byte chunk c of
+//     row r stored at chunk c ^ (r mod 8), the XOR swizzle of Q7) puts them
+//     in distinct banks;
+//   * B is N-major; a lane's columns are TNC chunks of 4 spaced 4 LANES_N
+//     apart, so the distinct lane columns of one load are contiguous
 //     (section 五.4's split-column fix of the 4-wavefront conflict);
 //   * zero-filled out-of-range loads plus predicated stores handle shapes
 //     that are not tile multiples (section 七).
@@ -39,26 +38,31 @@ namespace {
 
 constexpr int BM = kTileM, BN = kTileN, BK = kTileK, STAGES = kTileStages;
 constexpr int NT = kTileThreads;
-constexpr int TM = 8;                 // rows per lane
-constexpr int LANES_N = 4;            // lanes of a warp along N
-constexpr int LANES_M = 32 / LANES_N; // lanes along M (a lane's rows are
-                                      // LANES_M apart)
-constexpr int WM = LANES_M * TM;      // warp tile 64 x 32
-constexpr int WN = LANES_N * 8;
-constexpr int WARPS_N = BN / WN;      // 4 (2 along M)
-constexpr int COL_SPLIT = 4 * LANES_N;  // a lane's 2nd 4-column chunk offset
-constexpr int A_ROW = BK * 4;         // bytes per A row in shared memory
-constexpr int B_ROW = BN * 4;         // bytes per B row in shared memory
-constexpr int A_STAGE = BM * A_ROW;   // 16 KiB
-constexpr int B_STAGE = BK * B_ROW;   // 16 KiB
+constexpr int MIN_BLOCKS = kTileMinBlocks;
+constexpr int TM = kLaneRows;            // rows per lane
+constexpr int TNC = kLaneChunks;         // 4-column chunks per lane
+constexpr int TJ = 2 * TNC;              // column pairs per lane
+constexpr int LANES_N = kLanesN;         // lanes of a warp along N
+constexpr int LANES_M = 32 / LANES_N;    // lanes along M (rows LANES_M apart)
+constexpr int WM = LANES_M * TM;         // warp tile
+constexpr int WN = LANES_N * 4 * TNC;
+constexpr int WARPS_N = BN / WN;
+constexpr int WARPS_M = NT / 32 / WARPS_N;
+constexpr int COL_SPLIT = 4 * LANES_N;   // distance of a lane's column chunks
+constexpr int A_ROW = BK * 4;            // bytes per A row in shared memory
+constexpr int B_ROW = BN * 4;            // bytes per B row in shared memory
+constexpr int A_STAGE = BM * A_ROW;
+constexpr int B_STAGE = BK * B_ROW;
 constexpr int STAGE_TX = A_STAGE + B_STAGE;
-constexpr int GROUP_M = 8;            // grouped raster of the tile order
+constexpr int GROUP_M = 8;               // grouped raster of the tile order
 constexpr size_t SMEM_BYTES = size_t(STAGES) * STAGE_TX + 64 + 1024;
 
 static_assert(A_ROW == 128, "A rows are one 128-byte swizzle span");
-static_assert((BM / WM) * (BN / WN) * 32 == NT, "warp grid");
 static_assert(LANES_M * LANES_N == 32 && LANES_M <= 8 && 8 % LANES_M == 0,
               "lane grid");
+static_assert(WARPS_M * WM == BM && WARPS_N * WN == BN, "warp grid");
+static_assert(A_STAGE % 1024 == 0, "swizzled stages stay 1024-aligned");
+static_assert(BM <= 256 && BN <= 256, "TMA box limit");
 
 // Tile id -> (tile row, tile col) in groups of GROUP_M tile rows, column by
 // column inside a group, so blocks running together share A and B slices in
@@ -79,7 +83,7 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n,
 // a_rows: this lane's first A row in the stage (row r0; its rows are
 // r0 + LANES_M i); b_cols: this lane's first B column in row 0 of the stage;
 // lane_m: r0 mod LANES_M (r0 - lane_m is a multiple of 8).
-__device__ __forceinline__ void compute_slice(f2 (&acc)[TM][4],
+__device__ __forceinline__ void compute_slice(f2 (&acc)[TM][TJ],
                                               const uint8_t* a_rows,
                                               const uint8_t* b_cols,
                                               int lane_m) {
@@ -95,27 +99,36 @@ __device__ __forceinline__ void compute_slice(f2 (&acc)[TM][4],
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint8_t* brow = b_cols + (kq * 4 + kk) * B_ROW;
-      const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(brow);
-      const ulonglong2 b1 =
-          *reinterpret_cast<const ulonglong2*>(brow + 4 * COL_SPLIT);
-      const f2 bp0{b0.x}, bp1{b0.y}, bp2{b1.x}, bp3{b1.y};
+      f2 bp[TJ];
+#pragma unroll
+      for (int c = 0; c < TNC; ++c) {
+        const ulonglong2 b =
+            *reinterpret_cast<const ulonglong2*>(brow + 4 * COL_SPLIT * c);
+        bp[2 * c].v = b.x;
+        bp[2 * c + 1].v = b.y;
+      }
 #pragma unroll
       for (int i = 0; i < TM; ++i) {
         const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y
                        : kk == 2 ? a[i].z : a[i].w;
         const f2 ap = f2_pack(av, av);
-        f2_fma(acc[i][0], ap, bp0);
-        f2_fma(acc[i][1], ap, bp1);
-        f2_fma(acc[i][2], ap, bp2);
-        f2_fma(acc[i][3], ap, bp3);
+#pragma unroll
+        for (int j = 0; j < TJ; ++j) f2_fma(acc[i][j], ap, bp[j]);
       }
     }
   }
 }
 
-// Write the lane's 8 x 8 results. Row i of the lane is m0 + r0 + LANES_M i;
-// its columns are n0 + c0 + {0..3} and n0 + c0 + COL_SPLIT + {0..3}.
-__device__ __forceinline__ void store_tile(const f2 (&acc)[TM][4], float* C,
+__device__ __forceinline__ void zero_acc(f2 (&acc)[TM][TJ]) {
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TJ; ++j) acc[i][j].v = 0ull;
+}
+
+// Write the lane's results. Row i of the lane is m0 + r0 + LANES_M i; chunk
+// h covers columns n0 + c0 + COL_SPLIT h + {0..3}.
+__device__ __forceinline__ void store_tile(const f2 (&acc)[TM][TJ], float* C,
                                            int M, int N, long long ldc, int m0,
                                            int n0, int r0, int c0, bool vec) {
 #pragma unroll
@@ -124,7 +137,7 @@ __device__ __forceinline__ void store_tile(const f2 (&acc)[TM][4], float* C,
     if (r >= M) continue;
     float* crow = C + (long long)r * ldc;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < TNC; ++h) {
       const int c = n0 + c0 + COL_SPLIT * h;
       if (vec && c + 3 < N) {
         ulonglong2 v;
@@ -143,23 +156,12 @@ __device__ __forceinline__ void store_tile(const f2 (&acc)[TM][4], float* C,
   }
 }
 
-struct Geometry {
-  int m0, n0, r0, c0, lane_m, T;
-};
-
-__device__ __forceinline__ Geometry block_geometry(int M, int N, int K) {
-  Geometry g;
-  const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-  int pm, pn;
-  tile_coords(blockIdx.x, tiles_m, tiles_n, pm, pn);
-  g.m0 = pm * BM;
-  g.n0 = pn * BN;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  g.lane_m = lane / LANES_N;
-  g.r0 = (warp / WARPS_N) * WM + g.lane_m;
-  g.c0 = (warp % WARPS_N) * WN + (lane % LANES_N) * 4;
-  g.T = (K + BK - 1) / BK;
-  return g;
+// Per-lane offsets inside the block tile.
+__device__ __forceinline__ int lane_row0(int tid) {
+  return (tid >> 5) / WARPS_N * WM + (tid & 31) / LANES_N;
+}
+__device__ __forceinline__ int lane_col0(int tid) {
+  return (tid >> 5) % WARPS_N * WN + (tid % LANES_N) * 4;
 }
 
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
@@ -209,21 +211,22 @@ __device__ __forceinline__ int block_of(int x, const SkParams& p) {
 
 // Partial tiles are stored thread-major: value q of thread t at q * NT + t,
 // so the stores and loads of a block are fully coalesced 8-byte accesses.
-__device__ __forceinline__ void store_partial(const f2 (&acc)[TM][4],
+__device__ __forceinline__ void store_partial(const f2 (&acc)[TM][TJ],
                                               unsigned long long* w) {
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) __stcg(w + (i * 4 + j) * NT + threadIdx.x, acc[i][j].v);
+    for (int j = 0; j < TJ; ++j)
+      __stcg(w + (i * TJ + j) * NT + threadIdx.x, acc[i][j].v);
 }
 
-__device__ __forceinline__ void add_partial(f2 (&sum)[TM][4],
+__device__ __forceinline__ void add_partial(f2 (&sum)[TM][TJ],
                                             const unsigned long long* w) {
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const unsigned long long v = __ldcg(w + (i * 4 + j) * NT + threadIdx.x);
+    for (int j = 0; j < TJ; ++j) {
+      const unsigned long long v = __ldcg(w + (i * TJ + j) * NT + threadIdx.x);
       asm("add.rn.f32x2 %0, %0, %1;" : "+l"(sum[i][j].v) : "l"(v));
     }
 }
@@ -232,7 +235,7 @@ __device__ __forceinline__ void add_partial(f2 (&sum)[TM][4],
 // of this piece. Every piece, the last one included, goes through the
 // workspace, so the block that arrives last re-reads all pieces in piece
 // order and the sum does not depend on which block that is.
-__device__ __forceinline__ void sk_fixup(const f2 (&acc)[TM][4], int tile,
+__device__ __forceinline__ void sk_fixup(const f2 (&acc)[TM][TJ], int tile,
                                          int my_slot, const SkParams& p,
                                          float* C, int m0, int n0, int r0,
                                          int c0, int* s_flag) {
@@ -251,11 +254,8 @@ __device__ __forceinline__ void sk_fixup(const f2 (&acc)[TM][4], int tile,
   __syncthreads();  // s_flag is reused by the next segment
   if (arrived != pieces - 1) return;
   __threadfence();
-  f2 sum[TM][4];
-#pragma unroll
-  for (int i = 0; i < TM; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) sum[i][j].v = 0ull;
+  f2 sum[TM][TJ];
+  zero_acc(sum);
   for (int j = 0; j < pieces; ++j) {
     const int cj = c_first + j;
     // A block's piece of this tile is its first segment when its range
@@ -273,7 +273,7 @@ struct Producer {
   int kt, tile, m0, n0;
 };
 
-__global__ void __launch_bounds__(NT, 2)
+__global__ void __launch_bounds__(NT, MIN_BLOCKS)
 k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
             const __grid_constant__ CUtensorMap tmB, float* __restrict__ C,
             const SkParams p) {
@@ -325,16 +325,12 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
   }
   __syncthreads();
 
-  f2 acc[TM][4];
-#pragma unroll
-  for (int i = 0; i < TM; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j].v = 0ull;
+  f2 acc[TM][TJ];
+  zero_acc(acc);
 
   const int lane_m = (tid & 31) / LANES_N;
-  const uint8_t* a_rows = sA + ((tid >> 5) / WARPS_N * WM + lane_m) * A_ROW;
-  const uint8_t* b_cols =
-      sB + ((tid >> 5) % WARPS_N * WN + (tid % LANES_N) * 4) * 4;
+  const uint8_t* a_rows = sA + lane_row0(tid) * A_ROW;
+  const uint8_t* b_cols = sB + lane_col0(tid) * 4;
   int slot = 0;
   uint32_t phase = 0;
   int tile_end = (it_begin / I + 1) * I;  // end of the current tile's slices
@@ -370,27 +366,25 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
       const int tile_begin = tile_end - I;
       int pm, pn;
       tile_coords(tile, p.tiles_m, p.tiles_n, pm, pn);
-      const int warp = tid >> 5;
-      const int r0 = warp / WARPS_N * WM + lane_m;
-      const int c0 = warp % WARPS_N * WN + (tid % LANES_N) * 4;
       if (it_begin <= tile_begin && it + 1 == tile_end)
-        store_tile(acc, C, p.M, p.N, p.ldc, pm * BM, pn * BN, r0, c0,
-                   p.vec_store != 0);
+        store_tile(acc, C, p.M, p.N, p.ldc, pm * BM, pn * BN, lane_row0(tid),
+                   lane_col0(tid), p.vec_store != 0);
       else
         sk_fixup(acc, tile, 2 * blockIdx.x + (it_begin >= tile_begin ? 0 : 1),
-                 p, C, pm * BM, pn * BN, r0, c0, &s_flag);
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j].v = 0ull;
+                 p, C, pm * BM, pn * BN, lane_row0(tid), lane_col0(tid),
+                 &s_flag);
+      zero_acc(acc);
       tile_end += I;
     }
   }
 }
 
 // ------------------------------------------------------- cp.async kernel
+//
+// One block per output tile (no persistence), operands copied 4 bytes at a
+// time with zero-fill, into the same shared layouts as the TMA path.
 
-__global__ void __launch_bounds__(NT, 2)
+__global__ void __launch_bounds__(NT, MIN_BLOCKS)
 k_tiled_ldg(const float* __restrict__ A, long long lda,
             const float* __restrict__ B, long long ldb, float* __restrict__ C,
             int M, int N, int K, long long ldc, int vec_store) {
@@ -398,64 +392,74 @@ k_tiled_ldg(const float* __restrict__ A, long long lda,
   uint8_t* smem = aligned_smem(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
-  const Geometry g = block_geometry(M, N, K);
   const int tid = threadIdx.x;
+  const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+  int pm, pn;
+  tile_coords(blockIdx.x, tiles_m, tiles_n, pm, pn);
+  const int m0 = pm * BM, n0 = pn * BN;
+  const int T = (K + BK - 1) / BK;
 
-  // A: element e = tid + 256 q of the 128 x 32 slice is row (tid >> 5) + 8 q,
-  // column k = tid & 31, stored at the swizzled chunk (k / 4) ^ (row mod 8).
+  // A: element e = tid + NT q of the BM x 32 slice is row tid / 32 +
+  // (NT / 32) q, column k = tid mod 32, stored at the swizzled chunk
+  // (k / 4) ^ (row mod 8).
+  constexpr int A_ROWS_PER_PASS = NT / 32;
+  static_assert(A_ROWS_PER_PASS % 8 == 0, "row mod 8 fixed per thread");
   const int a_k = tid & 31, a_r = tid >> 5;
   const uint32_t a_dst = smem_u32(sA) + a_r * A_ROW +
-                         ((((a_k >> 2) ^ a_r) << 4) | ((a_k & 3) << 2));
-  // B: element e = tid + 256 q is k-row (tid >> 7) + 2 q, column tid & 127.
-  const int b_n = tid & 127, b_k = tid >> 7;
+                         ((((a_k >> 2) ^ (a_r & 7)) << 4) | ((a_k & 3) << 2));
+  // B: element e = tid + NT q is k-row tid / BN + (NT / BN) q, column
+  // tid mod BN.
+  constexpr int B_ROWS_PER_PASS = NT / BN;
+  static_assert(NT % BN == 0, "B rows per pass");
+  const int b_n = tid % BN, b_k = tid / BN;
   const uint32_t b_dst = smem_u32(sB) + b_k * B_ROW + b_n * 4;
-  const bool b_col_ok = g.n0 + b_n < N;
+  const bool b_col_ok = n0 + b_n < N;
 
   auto issue = [&](int tile, int slot) {
     const int k0 = tile * BK;
     const bool ak_ok = k0 + a_k < K;
 #pragma unroll
-    for (int q = 0; q < BM / 8; ++q) {
-      const int r = g.m0 + a_r + 8 * q;
+    for (int q = 0; q < BM / A_ROWS_PER_PASS; ++q) {
+      const int r = m0 + a_r + A_ROWS_PER_PASS * q;
       const bool ok = ak_ok && r < M;
       const float* src = ok ? A + (long long)r * lda + k0 + a_k : A;
-      cp_async_4(a_dst + slot * A_STAGE + q * 8 * A_ROW, src, ok ? 4u : 0u);
+      cp_async_4(a_dst + slot * A_STAGE + q * A_ROWS_PER_PASS * A_ROW, src,
+                 ok ? 4u : 0u);
     }
 #pragma unroll
-    for (int q = 0; q < BK / 2; ++q) {
-      const int kr = k0 + b_k + 2 * q;
+    for (int q = 0; q < BK / B_ROWS_PER_PASS; ++q) {
+      const int kr = k0 + b_k + B_ROWS_PER_PASS * q;
       const bool ok = b_col_ok && kr < K;
-      const float* src = ok ? B + (long long)kr * ldb + g.n0 + b_n : B;
-      cp_async_4(b_dst + slot * B_STAGE + q * 2 * B_ROW, src, ok ? 4u : 0u);
+      const float* src = ok ? B + (long long)kr * ldb + n0 + b_n : B;
+      cp_async_4(b_dst + slot * B_STAGE + q * B_ROWS_PER_PASS * B_ROW, src,
+                 ok ? 4u : 0u);
     }
   };
 
   for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < g.T) issue(s, s);
+    if (s < T) issue(s, s);
     cp_async_commit();
   }
 
-  f2 acc[TM][4];
-#pragma unroll
-  for (int i = 0; i < TM; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j].v = 0ull;
-
-  const uint8_t* a_rows = sA + g.r0 * A_ROW;
-  const uint8_t* b_cols = sB + g.c0 * 4;
+  f2 acc[TM][TJ];
+  zero_acc(acc);
+  const int lane_m = (tid & 31) / LANES_N;
+  const uint8_t* a_rows = sA + lane_row0(tid) * A_ROW;
+  const uint8_t* b_cols = sB + lane_col0(tid) * 4;
   int slot = 0;
-  for (int t = 0; t < g.T; ++t) {
+  for (int t = 0; t < T; ++t) {
     cp_async_wait<STAGES - 2>();  // this thread's copies of slice t landed
     __syncthreads();              // everyone's did; slice t-1 fully read
     const int nt = t + STAGES - 1;
-    if (nt < g.T) issue(nt, nt % STAGES);
+    if (nt < T) issue(nt, nt % STAGES);
     cp_async_commit();
     compute_slice(acc, a_rows + slot * A_STAGE, b_cols + slot * B_STAGE,
-                  g.lane_m);
+                  lane_m);
     if (++slot == STAGES) slot = 0;
   }
   cp_async_wait<0>();
-  store_tile(acc, C, M, N, ldc, g.m0, g.n0, g.r0, g.c0, vec_store != 0);
+  store_tile(acc, C, M, N, ldc, m0, n0, lane_row0(tid), lane_col0(tid),
+             vec_store != 0);
 }
 
 int grid_tiles(const GemmArgs& g) {
