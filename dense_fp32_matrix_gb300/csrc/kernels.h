@@ -65,7 +65,25 @@ cudaError_t launch_tiled_tma(const GemmArgs& g, const CUtensorMap& tmA,
 // alignment, any leading dimension).
 cudaError_t launch_tiled_ldg(const GemmArgs& g, int* status, cudaStream_t s);
 
-// M == 1 and N == 1 bandwidth kernels; one-thread-per-output kernel.
+// TMA-staged vector kernels (sgemm_gemv.cu). M == 1: B as dims {N, K}, box
+// {64, 64}, and a as a rank-1 map of K elements, box {64}; N == 1: A as dims {K, M}, box {256, 16}, and b as a rank-1 map
+// of K elements, box {256}. Need 16-byte aligned bases and row strides.
+struct GemvRowPlan {
+  int64_t col_blocks = 0;   // 64-column strips
+  int cluster = 1;          // blocks per strip (k-split), one cluster
+  int64_t k_per_block = 0;  // multiple of 64
+};
+cudaError_t gemv_tma_init();
+GemvRowPlan plan_gemv_row(int64_t N, int64_t K, int num_sms);
+cudaError_t launch_gemv_row_tma(const GemmArgs& g, const CUtensorMap& tmB,
+                                const CUtensorMap& tma_, const GemvRowPlan& pl,
+                                int* status, cudaStream_t s);
+cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
+                                const CUtensorMap& tmb, int* status,
+                                cudaStream_t s);
+
+// M == 1 and N == 1 bandwidth kernels for any layout; one-thread-per-output
+// kernel.
 cudaError_t launch_gemv_row(const GemmArgs& g, int num_sms, cudaStream_t s);
 cudaError_t launch_gemv_col(const GemmArgs& g, int num_sms, cudaStream_t s);
 cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s);

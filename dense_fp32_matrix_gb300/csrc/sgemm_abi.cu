@@ -83,7 +83,8 @@ void init_device(DeviceState& st) {
           cudaSuccess ||
       cudaMemset(st.status, 0, sizeof(int) * 4) != cudaSuccess ||
       tiled_init(&st.tma_blocks_per_sm) != cudaSuccess ||
-      st.tma_blocks_per_sm < 1 || small_init() != cudaSuccess) {
+      st.tma_blocks_per_sm < 1 || small_init() != cudaSuccess ||
+      gemv_tma_init() != cudaSuccess) {
     st.err = SGEMM_ERR_CUDA;
     return;
   }
@@ -207,6 +208,74 @@ int encode_maps(const GemmArgs& g, CUtensorMap* tmA, CUtensorMap* tmB) {
   return SGEMM_OK;
 }
 
+// Generic 2-D fp32 tensor map: dims {inner, outer}, row stride ld floats.
+int encode_2d(CUtensorMap* map, const float* base, int64_t inner,
+              int64_t outer, int64_t ld, uint32_t box_inner,
+              uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return SGEMM_ERR_CUDA;
+  const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+  const cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? SGEMM_OK
+             : SGEMM_ERR_CUDA;
+}
+
+int encode_1d(CUtensorMap* map, const float* base, int64_t n, uint32_t box) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return SGEMM_ERR_CUDA;
+  const cuuint64_t dims[1] = {cuuint64_t(n)};
+  const cuuint64_t unused_strides[1] = {cuuint64_t((n * 4 + 15) / 16 * 16)};
+  const cuuint32_t boxd[1] = {box};
+  const cuuint32_t estr[1] = {1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float*>(base),
+             dims, unused_strides, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? SGEMM_OK
+             : SGEMM_ERR_CUDA;
+}
+
+cudaError_t run_gemv_row(const GemmArgs& g, const DeviceState& st,
+                         cudaStream_t s, int* rc_out) {
+  *rc_out = SGEMM_OK;
+  if (tma_operand_ok(reinterpret_cast<uint64_t>(g.B), g.ldb) &&
+      reinterpret_cast<uint64_t>(g.A) % 16 == 0) {
+    CUtensorMap tmB, tma_;
+    int rc = encode_2d(&tmB, g.B, g.N, g.K, g.ldb, 64, 64);
+    if (rc == SGEMM_OK) rc = encode_1d(&tma_, g.A, g.K, 64);
+    if (rc != SGEMM_OK) {
+      *rc_out = rc;
+      return cudaSuccess;
+    }
+    return launch_gemv_row_tma(g, tmB, tma_, plan_gemv_row(g.N, g.K, st.sms),
+                               st.status, s);
+  }
+  return launch_gemv_row(g, st.sms, s);
+}
+
+cudaError_t run_gemv_col(const GemmArgs& g, const DeviceState& st,
+                         cudaStream_t s, int* rc_out) {
+  *rc_out = SGEMM_OK;
+  if (tma_operand_ok(reinterpret_cast<uint64_t>(g.A), g.lda) && g.ldb == 1 &&
+      reinterpret_cast<uint64_t>(g.B) % 16 == 0) {
+    CUtensorMap tmA, tmb;
+    int rc = encode_2d(&tmA, g.A, g.K, g.M, g.lda, 256, 16);
+    if (rc == SGEMM_OK) rc = encode_1d(&tmb, g.B, g.K, 256);
+    if (rc != SGEMM_OK) {
+      *rc_out = rc;
+      return cudaSuccess;
+    }
+    return launch_gemv_col_tma(g, tmA, tmb, st.status, s);
+  }
+  return launch_gemv_col(g, st.sms, s);
+}
+
 int to_status(cudaError_t e) {
   if (e == cudaSuccess) return SGEMM_OK;
   return (e == cudaErrorLaunchFailure || e == cudaErrorInvalidConfiguration ||
@@ -258,12 +327,16 @@ int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
     }
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
-    case SGEMM_PATH_GEMV_ROW:
+    case SGEMM_PATH_GEMV_ROW: {
       if (M != 1) return SGEMM_ERR_PATH;
-      return to_status(launch_gemv_row(g, st->sms, s));
-    case SGEMM_PATH_GEMV_COL:
+      const cudaError_t e = run_gemv_row(g, *st, s, &rc);
+      return rc != SGEMM_OK ? rc : to_status(e);
+    }
+    case SGEMM_PATH_GEMV_COL: {
       if (N != 1) return SGEMM_ERR_PATH;
-      return to_status(launch_gemv_col(g, st->sms, s));
+      const cudaError_t e = run_gemv_col(g, *st, s, &rc);
+      return rc != SGEMM_OK ? rc : to_status(e);
+    }
     case SGEMM_PATH_NAIVE:
       return to_status(launch_naive(g, s));
     default:
@@ -313,10 +386,14 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
     }
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
-    case SGEMM_PATH_GEMV_ROW:
-      return to_status(launch_gemv_row(g, st->sms, s));
-    case SGEMM_PATH_GEMV_COL:
-      return to_status(launch_gemv_col(g, st->sms, s));
+    case SGEMM_PATH_GEMV_ROW: {
+      const cudaError_t e = run_gemv_row(g, *st, s, &rc);
+      return rc != SGEMM_OK ? rc : to_status(e);
+    }
+    case SGEMM_PATH_GEMV_COL: {
+      const cudaError_t e = run_gemv_col(g, *st, s, &rc);
+      return rc != SGEMM_OK ? rc : to_status(e);
+    }
     default:
       return SGEMM_ERR_PATH;
   }

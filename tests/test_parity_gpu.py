@@ -56,16 +56,21 @@ def test_brute_force_tiny_shapes(path):
                  path=path, check="full")
 
 
+# (1, 1000, 777), (1, 20, 3), (1, 4096, 4096): 16-byte row strides, TMA
+# kernel with a cluster k-split; (1, 17, 3), (1, 1, 5000): plain kernel.
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (1, 1000, 777),
-                                   (1, 1, 5000), (1, 17, 3)])
+                                   (1, 1, 5000), (1, 17, 3), (1, 20, 3),
+                                   (1, 4100, 65), (1, 64, 11008)])
 def test_gemv_row(M, N, K):
     for kind in ("uniform", "integers"):
         run_case(M, N, K, kind=kind, seed=K, path="gemv_row")
     run_case(M, N, K, kind="uniform", seed=K, path="gemv_row", ldb=N + 5)
 
 
+# K % 4 == 0 with ldb == 1: TMA kernel; otherwise the plain kernel.
 @pytest.mark.parametrize("M,N,K", [(4096, 1, 4096), (1000, 1, 777),
-                                   (3, 1, 5000), (17, 1, 3)])
+                                   (3, 1, 5000), (17, 1, 3), (1000, 1, 780),
+                                   (33, 1, 260), (4097, 1, 11008)])
 def test_gemv_col(M, N, K):
     for kind in ("uniform", "integers"):
         run_case(M, N, K, kind=kind, seed=K, path="gemv_col")
