@@ -36,6 +36,10 @@ sys.path.insert(0, ROOT)
 FMA_PER_CLK_PER_SM = 128   # FP32 FMA lanes per SM (4 SMSPs x 32)
 L2_FLUSH_BYTES = 256 << 20
 CPU_SAMPLE_SECONDS = 12.0
+# Nominal dense tensor rates per GPU: TF32 1.1 PFLOP/s, BF16 2.25 PFLOP/s.
+TF32_PER_BF16 = 1.1 / 2.25
+BF16_FALLBACK_TFLOPS = 1900.0   # used only when no measured peak is present
+TF32X3_PRODUCTS = 3             # TF32 tensor products per fp32 product
 
 
 def flops(M, N, K):
@@ -46,13 +50,20 @@ def algorithmic_bytes(M, N, K):
     return 4.0 * (M * K + K * N + M * N)
 
 
-def source_digest():
+# Source files that define each kernel (its traffic record is valid only
+# while these are unchanged).
+KERNEL_SOURCES = {
+    "k_tiled_tma": ["sgemm_tiled.cu", "ptx.cuh", "kernels.h"],
+    "k_tf32x3": ["sgemm_tf32x3.cu", "tcgen05.cuh", "ptx.cuh", "kernels.h"],
+}
+
+
+def source_digest(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp32_matrix_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
@@ -65,7 +76,9 @@ def recorded_traffic(kernel, workload):
             recs = json.load(f)
     except (OSError, ValueError):
         return None
-    digest = source_digest()
+    if kernel not in KERNEL_SOURCES:
+        return None
+    digest = source_digest(kernel)
     for r in recs.get("records", []):
         if (r.get("kernel") == kernel and r.get("workload") == workload
                 and r.get("source_sha256") == digest):
@@ -136,6 +149,34 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm),
                 "power_w_max": max(power) if power else None}
+
+
+def measured_bf16_tflops():
+    """(bf16 dense TFLOP/s burst, source) from MEASURED_PEAKS.json."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured"
+    except (OSError, ValueError, KeyError):
+        return BF16_FALLBACK_TFLOPS, "fallback"
+
+
+def time_steps(step, flush, stream, n, warmup):
+    """Per-step device times (ms) with an L2 flush before each step."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
 
 
 def dist_env():
@@ -321,24 +362,52 @@ def run_gpu(args, w):
     if not torch.equal(hC, C.cpu()):
         raise RuntimeError("e2e result differs from the device-path result")
 
-    peak_clock_mhz = clk["sm_mhz"] or (clk["sm_max_mhz"] or None)
-    roof = None
-    if peak_clock_mhz:
-        peak = sms * FMA_PER_CLK_PER_SM * 2 * peak_clock_mhz * 1e6 / 1e12
-        kernel = {"tiled_tma": "k_tiled_tma", "tiled_ldg": "k_tiled_ldg"}.get(
-            plan, plan)
-        roof = {"bound": "alu", "achieved": tflops, "peak": peak,
-                "unit": "TFLOP/s", "frac": tflops / peak,
+    # The FP32 FMA roofline of this GPU at the clock seen while timing.
+    peak_clock_mhz = clk["sm_mhz"] or (clk["sm_max_mhz"] or 2070.0)
+    ffma_peak = sms * FMA_PER_CLK_PER_SM * 2 * peak_clock_mhz * 1e6 / 1e12
+    ffma_basis = ("%d SMs x %d FP32 FMA/clk x 2 flop x %.0f MHz (median SM "
+                  "clock sampled during the timed region)"
+                  % (sms, FMA_PER_CLK_PER_SM, peak_clock_mhz))
+    kernel = {"tiled_tma": "k_tiled_tma", "tiled_ldg": "k_tiled_ldg",
+              "tf32x3": "k_tf32x3"}.get(plan, plan)
+    if plan == "tf32x3":
+        bf16, src = measured_bf16_tflops()
+        tf32_peak = bf16 * TF32_PER_BF16
+        eff_peak = tf32_peak / TF32X3_PRODUCTS
+        roof = {"bound": "tensor", "achieved": tflops, "peak": eff_peak,
+                "unit": "TFLOP/s", "frac": tflops / eff_peak,
                 "traffic": recorded_traffic(kernel, w["name"]),
                 "kernel": kernel,
-                "peak_basis": ("%d SMs x %d FP32 FMA/clk x 2 flop x %.0f MHz "
-                               "(median SM clock sampled during the timed "
-                               "region)" % (sms, FMA_PER_CLK_PER_SM,
-                                            peak_clock_mhz))}
-        if clk["sm_max_mhz"]:
-            pmax = sms * FMA_PER_CLK_PER_SM * 2 * clk["sm_max_mhz"] * 1e6 / 1e12
-            roof["peak_at_max_clock"] = pmax
-            roof["frac_at_max_clock"] = tflops / pmax
+                "peak_basis": ("TF32 dense tensor peak = bf16 burst %.1f "
+                               "TFLOP/s (%s, MEASURED_PEAKS.json) x nominal "
+                               "TF32/BF16 ratio 1.1/2.25 = %.1f TFLOP/s; "
+                               "3 TF32 products per fp32 product -> %.1f "
+                               "TFLOP/s of fp32 work" % (bf16, src, tf32_peak,
+                                                         eff_peak)),
+                "tensor_tflops": TF32X3_PRODUCTS * tflops,
+                "tensor_peak": tf32_peak}
+    else:
+        roof = {"bound": "alu", "achieved": tflops, "peak": ffma_peak,
+                "unit": "TFLOP/s", "frac": tflops / ffma_peak,
+                "traffic": recorded_traffic(kernel, w["name"]),
+                "kernel": kernel, "peak_basis": ffma_basis}
+
+    # The CUDA-core FFMA kernel on the same inputs, timed the same way.
+    ffma = None
+    if plan == "tf32x3" and not args.no_ffma:
+        prev = dfm.sgemm_set_math_mode("ffma")
+        try:
+            ffma_path = dfm.sgemm_plan(M, N, K, K, N, N, A.data_ptr(),
+                                       B.data_ptr(), C.data_ptr())
+            fms = time_steps(step, flush, stream, max(5, min(args.steps, 100)),
+                             args.warmup)
+        finally:
+            dfm.sgemm_set_math_mode(prev)
+        f_ms = sum(fms) / len(fms)
+        f_tflops = flops(M, N, K) / (f_ms * 1e-3) / 1e12
+        ffma = {"path": ffma_path, "value": f_tflops * world,
+                "ms_per_step": f_ms, "frac_of_ffma_peak": f_tflops / ffma_peak,
+                "traffic": recorded_traffic("k_tiled_tma", w["name"])}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -347,10 +416,17 @@ def run_gpu(args, w):
         "dtype": "f32", "data": "synthetic",
         "config": config_of(w, extra={
             "path": plan, "sms": sms, "gpu": props.name,
+            "arithmetic": ("3xTF32 tensor-core products (hi/lo split), fp32 "
+                           "accumulation" if plan == "tf32x3" else
+                           "fp32 fused multiply-add on CUDA cores"),
             "l2": "flushed before every step (256 MiB device memset, "
                   "outside the timed events)",
             "parallelism": "replicas" if world > 1 else "single GPU"}),
         "roofline": roof,
+        "pct_of_ffma_peak": 100.0 * tflops / ffma_peak,
+        "ffma_peak": {"value": ffma_peak, "unit": "TFLOP/s",
+                      "basis": ffma_basis},
+        "ffma_kernel": ffma,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
                    "reasons": clk["reasons"], "samples": clk["samples"],
                    "power_w_max": clk.get("power_w_max")},
@@ -389,6 +465,8 @@ def main(argv=None):
     p.add_argument("--path", default="auto",
                    help="force a kernel path (auto, tiled_tma, tiled_ldg, ...)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-ffma", action="store_true",
+                   help="skip timing the CUDA-core kernel beside the tensor one")
     args = p.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     from matgen import workloads

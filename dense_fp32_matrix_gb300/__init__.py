@@ -13,7 +13,7 @@ from . import _native
 
 __all__ = [
     "SgemmError", "sgemm", "sgemm_path", "sgemm_plan", "sgemm_host",
-    "sgemm_noalloc",
+    "sgemm_noalloc", "sgemm_set_math_mode", "MATH",
     "sgemm_watchdog_status", "sgemm_watchdog_selftest",
     "sgemm_status_string", "sgemm_path_name", "sgemm_version", "matmul",
     "PATHS", "STATUS",
@@ -25,8 +25,9 @@ STATUS = {
     "SGEMM_ERR_WATCHDOG": -5, "SGEMM_ERR_OVERLAP": -6, "SGEMM_ERR_CUDA": -7,
     "SGEMM_ERR_PATH": -8, "SGEMM_ERR_TOO_LARGE": -9,
 }
+MATH = {"auto": 0, "ffma": 1}
 PATHS = {"auto": 0, "tiled_tma": 1, "tiled_ldg": 2, "gemv_row": 3,
-         "gemv_col": 4, "naive": 5}
+         "gemv_col": 4, "naive": 5, "tf32x3": 6}
 
 
 class SgemmError(RuntimeError):
@@ -83,6 +84,15 @@ def sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> None:
     _check(_native.lib().sgemm_noalloc(M, N, K, _ptr(A), lda, _ptr(B), ldb,
                                        _ptr(C), ldc, _stream(stream)),
            "sgemm_noalloc")
+
+
+def sgemm_set_math_mode(mode) -> str:
+    """Process-wide math mode ("auto" or "ffma"); returns the previous one."""
+    m = MATH[mode] if isinstance(mode, str) else int(mode)
+    rc = int(_native.lib().sgemm_set_math_mode(m))
+    if rc < 0:
+        raise SgemmError(rc, "sgemm_set_math_mode")
+    return {v: k for k, v in MATH.items()}[rc]
 
 
 def sgemm_plan(M, N, K, lda, ldb, ldc, a_addr, b_addr, c_addr) -> str:

@@ -32,6 +32,7 @@ _SIGNATURES = {
                       _int),
     "sgemm_host": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp,
                     _vp, _vp, _vp], _int),
+    "sgemm_set_math_mode": ([_int], _int),
     "sgemm_watchdog_status": ([ctypes.POINTER(_int)], _int),
     "sgemm_watchdog_selftest": ([_vp, _i64], _int),
     "sgemm_status_string": ([_int], ctypes.c_char_p),

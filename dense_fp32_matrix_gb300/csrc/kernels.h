@@ -82,6 +82,13 @@ cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
                                 const CUtensorMap& tmb, int* status,
                                 cudaStream_t s);
 
+// 3xTF32 tensor-core kernel (sgemm_tf32x3.cu). tmA: A as dims {K, M}, box
+// {32, 128}, 128-byte swizzle; tmB: B as dims {N, K}, box {32, 32}, 128-byte
+// swizzle. Needs 16-byte aligned bases and row strides.
+cudaError_t tf32x3_init();
+cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
+                          const CUtensorMap& tmB, int* status, cudaStream_t s);
+
 // M == 1 and N == 1 bandwidth kernels for any layout; one-thread-per-output
 // kernel.
 cudaError_t launch_gemv_row(const GemmArgs& g, int num_sms, cudaStream_t s);

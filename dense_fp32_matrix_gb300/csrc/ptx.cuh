@@ -27,6 +27,10 @@ enum WaitSite : int {
   kSiteTiledDrain = 3,
   kSiteGemvRow = 4,
   kSiteGemvCol = 5,
+  kSiteTf32Full = 6,
+  kSiteTf32Conv = 7,
+  kSiteTf32Empty = 8,
+  kSiteTf32Acc = 9,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

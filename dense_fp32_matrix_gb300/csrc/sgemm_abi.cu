@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "dfm_sgemm.h"
@@ -19,6 +20,11 @@ namespace {
 __device__ int g_status[4];
 
 constexpr int kMaxDevices = 64;
+std::atomic<int> g_math_mode{SGEMM_MATH_AUTO};
+// Below this many 128 x 128 tiles with K this long, the stream-K CUDA-core
+// kernel (which splits K over all SMs) beats one tensor-core block per tile.
+constexpr int64_t kTf32MinTiles = 64;
+constexpr int64_t kTf32LongK = 2048;
 // Largest M, N or K the int-indexed kernels accept (tile rounding included).
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1024;
 
@@ -84,7 +90,7 @@ void init_device(DeviceState& st) {
       cudaMemset(st.status, 0, sizeof(int) * 4) != cudaSuccess ||
       tiled_init(&st.tma_blocks_per_sm) != cudaSuccess ||
       st.tma_blocks_per_sm < 1 || small_init() != cudaSuccess ||
-      gemv_tma_init() != cudaSuccess) {
+      gemv_tma_init() != cudaSuccess || tf32x3_init() != cudaSuccess) {
     st.err = SGEMM_ERR_CUDA;
     return;
   }
@@ -171,8 +177,14 @@ int plan_path(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
   const int64_t iters = ((M + kTileM - 1) / kTileM) *
                         ((N + kTileN - 1) / kTileN) *
                         ((K + kTileK - 1) / kTileK);
-  if (tma_operand_ok(a, lda) && tma_operand_ok(b, ldb) && iters < (1ll << 31))
+  if (tma_operand_ok(a, lda) && tma_operand_ok(b, ldb) && iters < (1ll << 31)) {
+    const int64_t tiles = ((M + kTileM - 1) / kTileM) *
+                          ((N + kTileN - 1) / kTileN);
+    if (g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO &&
+        !(tiles < kTf32MinTiles && K >= kTf32LongK))
+      return SGEMM_PATH_TF32X3;
     return SGEMM_PATH_TILED_TMA;
+  }
   return SGEMM_PATH_TILED_LDG;
 }
 
@@ -211,7 +223,8 @@ int encode_maps(const GemmArgs& g, CUtensorMap* tmA, CUtensorMap* tmB) {
 // Generic 2-D fp32 tensor map: dims {inner, outer}, row stride ld floats.
 int encode_2d(CUtensorMap* map, const float* base, int64_t inner,
               int64_t outer, int64_t ld, uint32_t box_inner,
-              uint32_t box_outer) {
+              uint32_t box_outer,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return SGEMM_ERR_CUDA;
   const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
@@ -219,8 +232,8 @@ int encode_2d(CUtensorMap* map, const float* base, int64_t inner,
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base),
-             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
              ? SGEMM_OK
              : SGEMM_ERR_CUDA;
@@ -284,6 +297,17 @@ int to_status(cudaError_t e) {
              : SGEMM_ERR_CUDA;
 }
 
+int run_tf32x3(const GemmArgs& g, const DeviceState& st, cudaStream_t s) {
+  CUtensorMap tmA, tmB;
+  int rc = encode_2d(&tmA, g.A, g.K, g.M, g.lda, 32, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == SGEMM_OK)
+    rc = encode_2d(&tmB, g.B, g.N, g.K, g.ldb, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != SGEMM_OK) return rc;
+  return to_status(launch_tf32x3(g, tmA, tmB, st.status, s));
+}
+
 int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
         const float* B, int64_t ldb, float* C, int64_t ldc, void* stream,
         int path) {
@@ -339,6 +363,10 @@ int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
     }
     case SGEMM_PATH_NAIVE:
       return to_status(launch_naive(g, s));
+    case SGEMM_PATH_TF32X3:
+      if (!tma_operand_ok(a, lda) || !tma_operand_ok(b, ldb))
+        return SGEMM_ERR_PATH;
+      return run_tf32x3(g, *st, s);
     default:
       return SGEMM_ERR_PATH;
   }
@@ -386,6 +414,8 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
     }
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
+    case SGEMM_PATH_TF32X3:
+      return run_tf32x3(g, *st, s);
     case SGEMM_PATH_GEMV_ROW: {
       const cudaError_t e = run_gemv_row(g, *st, s, &rc);
       return rc != SGEMM_OK ? rc : to_status(e);
@@ -412,6 +442,12 @@ int sgemm_path(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                const float* B, int64_t ldb, float* C, int64_t ldc,
                void* stream, int path) {
   return dfm::run(M, N, K, A, lda, B, ldb, C, ldc, stream, path);
+}
+
+int sgemm_set_math_mode(int mode) {
+  if (mode != SGEMM_MATH_AUTO && mode != SGEMM_MATH_FFMA)
+    return SGEMM_ERR_INVALID_VALUE;
+  return dfm::g_math_mode.exchange(mode);
 }
 
 int sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -515,6 +551,7 @@ const char* sgemm_path_name(int path) {
     case SGEMM_PATH_GEMV_ROW: return "gemv_row";
     case SGEMM_PATH_GEMV_COL: return "gemv_col";
     case SGEMM_PATH_NAIVE: return "naive";
+    case SGEMM_PATH_TF32X3: return "tf32x3";
     default: return "?";
   }
 }

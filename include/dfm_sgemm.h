@@ -22,10 +22,20 @@
  *   - C is overwritten (alpha = 1, beta = 0). Elements of C outside
  *     i < M, j < N (the pitch padding ldc > N) are never written. A and B
  *     are only read inside their logical extent (never in the padding).
- *   - Summation is in fp32 with fused multiply-add, k in an implementation
- *     order; results are deterministic run to run for a given shape, layout
- *     and path. On integer-valued inputs whose partial sums stay below 2^24
- *     in magnitude the result is exact.
+ *   - Accuracy contract: every element satisfies
+ *       |C_ij - sum_k A_ik B_kj| <= 1e-4 * sum_k |A_ik B_kj| + 1e-6
+ *     and results are exact on integer-valued inputs whose partial sums stay
+ *     below 2^24 in magnitude. Results are deterministic run to run for a
+ *     given shape, layout, path and device.
+ *   - Arithmetic: the CUDA-core paths use one fp32 fused multiply-add per
+ *     product (k in an implementation order). The tensor-core path
+ *     (SGEMM_PATH_TF32X3, chosen by sgemm for 16-byte-aligned operands in
+ *     SGEMM_MATH_AUTO) splits each operand x = hi + lo into TF32 parts and
+ *     sums A_lo B_hi + A_hi B_lo + A_hi B_hi in fp32: each product carries a
+ *     relative error below about 3 * 2^-20, well inside the contract. An
+ *     Inf input comes out as NaN on that path (Inf times a zero residual).
+ *     sgemm_set_math_mode(SGEMM_MATH_FFMA) restricts sgemm to the CUDA-core
+ *     paths.
  *   - M == 0 or N == 0: nothing is done. K == 0: C[0:M, 0:N] is set to 0.
  *   - NaN / Inf inputs propagate as IEEE fp32 arithmetic gives them.
  *
@@ -68,6 +78,10 @@ extern "C" {
 #define SGEMM_ERR_PATH (-8)             /* forced path cannot take the call */
 #define SGEMM_ERR_TOO_LARGE (-9)        /* size beyond a path's limit      */
 
+/* Math modes (sgemm_set_math_mode). */
+#define SGEMM_MATH_AUTO 0  /* fastest path within the accuracy contract     */
+#define SGEMM_MATH_FFMA 1  /* CUDA-core fp32 fused multiply-add paths only   */
+
 /* Kernel paths (sgemm_path / sgemm_plan). */
 #define SGEMM_PATH_AUTO 0
 #define SGEMM_PATH_TILED_TMA 1  /* TMA-fed multistage tile kernel (aligned) */
@@ -75,7 +89,8 @@ extern "C" {
 #define SGEMM_PATH_GEMV_ROW 3   /* M == 1: c = a * B, column blocks       */
 #define SGEMM_PATH_GEMV_COL 4   /* N == 1: c = A * b, one warp per row     */
 #define SGEMM_PATH_NAIVE 5      /* one thread per output (debug baseline)  */
-#define SGEMM_PATH_COUNT 6
+#define SGEMM_PATH_TF32X3 6     /* tensor cores, 3 TF32 products (aligned)  */
+#define SGEMM_PATH_COUNT 7
 
 /*
  * sgemm: C = A * B as described above, on `stream`.
@@ -101,8 +116,15 @@ int sgemm_path(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                void* stream, int path);
 
 /*
- * sgemm_plan: the path sgemm would take for these arguments, decided on the
- * host only (no device is touched). a_addr / b_addr / c_addr are the pointer
+ * sgemm_set_math_mode: SGEMM_MATH_AUTO (default) or SGEMM_MATH_FFMA, for the
+ * whole process, for calls that start after it returns. Returns the previous
+ * mode, or SGEMM_ERR_INVALID_VALUE for an unknown mode.
+ */
+int sgemm_set_math_mode(int mode);
+
+/*
+ * sgemm_plan: the path sgemm would take for these arguments (in the current
+ * math mode), decided on the host only (no device is touched). a_addr / b_addr / c_addr are the pointer
  * values (only their alignment is used). Writes the SGEMM_PATH_* value to
  * *path. Returns the same argument errors as sgemm (no device errors).
  */

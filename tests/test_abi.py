@@ -28,6 +28,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("sgemm", "sgemm_path", "sgemm_plan", "sgemm_host",
+              "sgemm_set_math_mode",
               "sgemm_watchdog_status", "sgemm_watchdog_selftest",
               "sgemm_status_string", "sgemm_path_name", "sgemm_version"):
         assert n in names
@@ -62,12 +63,13 @@ C16 = 0x7f0020000000
 
 
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc,a,b,expect", [
-    (4096, 4096, 4096, 4096, 4096, 4096, A16, B16, "tiled_tma"),
-    (256, 256, 256, 256, 256, 256, A16, B16, "tiled_tma"),
+    (4096, 4096, 4096, 4096, 4096, 4096, A16, B16, "tf32x3"),
+    (256, 256, 256, 256, 256, 256, A16, B16, "tf32x3"),
+    (512, 512, 4096, 4096, 512, 512, A16, B16, "tiled_tma"),  # few tiles, long K
     (4095, 4097, 1023, 1023, 4097, 4097, A16, B16, "tiled_ldg"),  # ld % 4
     (127, 129, 33, 33, 129, 129, A16, B16, "tiled_ldg"),
     (4096, 4096, 4096, 4096, 4096, 4096, A16 + 4, B16, "tiled_ldg"),  # align
-    (4096, 4096, 4096, 4100, 4096, 4096, A16, B16, "tiled_tma"),  # pitch
+    (4096, 4096, 4096, 4100, 4096, 4096, A16, B16, "tf32x3"),  # pitch
     (1, 4096, 4096, 4096, 4096, 4096, A16, B16, "gemv_row"),
     (4096, 1, 4096, 4096, 1, 1, A16, B16, "gemv_col"),
     (1, 1, 7, 7, 1, 1, A16, B16, "gemv_row"),
@@ -76,6 +78,19 @@ C16 = 0x7f0020000000
 ])
 def test_plan(lib, M, N, K, lda, ldb, ldc, a, b, expect):
     assert dfm.sgemm_plan(M, N, K, lda, ldb, ldc, a, b, C16) == expect
+
+
+def test_math_mode_restricts_to_cuda_cores(lib):
+    assert dfm.sgemm_set_math_mode("ffma") == "auto"
+    try:
+        assert dfm.sgemm_plan(4096, 4096, 4096, 4096, 4096, 4096, A16, B16,
+                              C16) == "tiled_tma"
+    finally:
+        assert dfm.sgemm_set_math_mode("auto") == "ffma"
+    assert dfm.sgemm_plan(4096, 4096, 4096, 4096, 4096, 4096, A16, B16,
+                          C16) == "tf32x3"
+    with pytest.raises(dfm.SgemmError):
+        dfm.sgemm_set_math_mode(7)
 
 
 @pytest.mark.parametrize("args,code", [

@@ -17,8 +17,14 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
+    # This module covers the CUDA-core fp32 FMA paths: "auto" here resolves
+    # to them (the tensor-core path has its own module).
+    import dense_fp32_matrix_gb300 as dfm
     from dense_fp32_matrix_gb300 import build
     build.build()
+    previous = dfm.sgemm_set_math_mode("ffma")
+    yield
+    dfm.sgemm_set_math_mode(previous)
 
 
 @pytest.mark.parametrize("w", WORKLOADS, ids=lambda w: w["name"])

@@ -1,0 +1,113 @@
+"""Parity of the 3xTF32 tensor-core path with the CPU oracle (C ABI).
+
+Same bar as every other path: bit-exact on integer data (the split leaves
+lo = 0 and TF32 products of small integers are exact), |C - C_oracle| <=
+1e-4 * S + 1e-6 otherwise. The path needs 16-byte row strides (K and N
+multiples of 4 for dense matrices)."""
+import itertools
+
+import numpy as np
+import pytest
+
+import matgen
+from matgen.workloads import WORKLOADS
+from gpu_util import run_case
+
+pytestmark = pytest.mark.gpu
+
+PATH = "tf32x3"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dense_fp32_matrix_gb300 import build
+    build.build()
+
+
+ALIGNED = [w for w in WORKLOADS if w["K"] % 4 == 0 and w["N"] % 4 == 0]
+
+
+@pytest.mark.parametrize("w", ALIGNED, ids=lambda w: w["name"])
+def test_workload(w):
+    worst = run_case(w["M"], w["N"], w["K"], w["kind"], w["seed"], path=PATH)
+    if w["kind"] != "integers":
+        # the split's extra error is ~3 * 2^-20 of each |product|
+        assert worst < 0.25
+
+
+@pytest.mark.parametrize("mnk", [(300, 200, 20), (260, 132, 36), (129, 260, 68),
+                                 (1000, 1000, 1000), (128, 128, 32),
+                                 (384, 256, 24), (1, 4096, 256), (4096, 4, 64)],
+                         ids=str)
+@pytest.mark.parametrize("kind", ["uniform", "integers", "normal"])
+def test_multi_tile(mnk, kind):
+    run_case(*mnk, kind=kind, seed=sum(mnk), path=PATH)
+
+
+def test_tiny_aligned_shapes_bit_exact():
+    for M, N, K in itertools.product((1, 2, 3, 5, 8, 17, 33, 129),
+                                     (4, 8, 12, 36, 132), (4, 8, 12, 36, 68)):
+        run_case(M, N, K, kind="integers", seed=M * 7 + N * 3 + K, path=PATH,
+                 check="full")
+
+
+def test_pitch_padding_never_read_or_written():
+    run_case(300, 200, 64, "uniform", 9, lda=72, ldb=204, ldc=260, path=PATH)
+    run_case(260, 132, 36, "integers", 9, lda=40, ldb=136, ldc=133, path=PATH)
+
+
+def test_unaligned_layout_is_refused():
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    buf = torch.zeros(1 << 16, device="cuda")
+    p = buf.data_ptr()
+    with pytest.raises(dfm.SgemmError) as e:
+        dfm.sgemm_path(64, 64, 33, p, 33, p + 4 * 8192, 64, p + 4 * 32768, 64,
+                       path=PATH)
+    assert e.value.status == dfm.STATUS["SGEMM_ERR_PATH"]
+
+
+def test_nan_and_inf_propagate():
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    A = torch.from_numpy(matgen.uniform(1, 0, 256, 256)).cuda()
+    B = torch.from_numpy(matgen.uniform(1, 1, 256, 256)).cuda()
+    A[7, 100] = float("nan")
+    B[30, 200] = float("nan")
+    C = dfm.matmul(A, B, path=PATH)
+    torch.cuda.synchronize()
+    nan = torch.isnan(C).cpu().numpy()
+    assert nan[7].all() and nan[:, 200].all()
+    nan[7] = False
+    nan[:, 200] = False
+    assert not nan.any()
+    # An infinite input makes its row non-finite. (On this path it comes out
+    # as NaN, not inf: the compensation term A_hi * B_lo multiplies the
+    # infinity by an exactly-zero residual.)
+    A = torch.ones(128, 128, device="cuda")
+    A[3, 5] = float("inf")
+    C = dfm.matmul(A, torch.ones(128, 128, device="cuda"), path=PATH)
+    torch.cuda.synchronize()
+    assert not torch.isfinite(C[3]).any()
+    assert torch.isfinite(C[:3]).all() and torch.isfinite(C[4:]).all()
+
+
+def test_auto_dispatch_picks_the_tensor_path_for_aligned_operands():
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    A = torch.from_numpy(matgen.integers(3, 0, 640, 388)).cuda()
+    B = torch.from_numpy(matgen.integers(3, 1, 388, 260)).cuda()
+    assert dfm.sgemm_plan(640, 260, 388, 388, 260, 260, A.data_ptr(),
+                          B.data_ptr(), 0x7f0020000000) == PATH
+    run_case(640, 260, 388, "integers", 3, path="auto")
+
+
+def test_deterministic():
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    A = torch.from_numpy(matgen.uniform(2, 0, 1000, 780)).cuda()
+    B = torch.from_numpy(matgen.uniform(2, 1, 780, 996)).cuda()
+    C1 = dfm.matmul(A, B, path=PATH)
+    C2 = dfm.matmul(A, B, path=PATH)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)

@@ -23,12 +23,23 @@ REL, ABS = 1e-4, 1e-6
 def lib():
     from dense_fp32_matrix_gb300 import _native, build
     build.build()
-    return _native.lib()
+    L = _native.lib()
+    return L
 
 
 def _call(fn, M, N, K, A, B, C, stream):
     rc = fn(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, stream)
     assert rc == 0, rc
+
+
+@pytest.fixture(params=["ffma", "auto"])
+def math_mode(request, lib):
+    # "ffma" routes aligned shapes to the stream-K kernel, the one that uses
+    # the fixed scratch; "auto" to the tensor-core kernel (no scratch).
+    modes = {"auto": 0, "ffma": 1}
+    previous = lib.sgemm_set_math_mode(modes[request.param])
+    yield request.param
+    lib.sgemm_set_math_mode(previous)
 
 
 @pytest.mark.parametrize("M,N,K,kind", [
@@ -38,7 +49,7 @@ def _call(fn, M, N, K, A, B, C, stream):
     (300, 200, 20, "uniform"),
     (127, 129, 33, "integers"),   # unaligned: a path without scratch
 ])
-def test_noalloc_matches_sgemm_on_two_calls(lib, M, N, K, kind):
+def test_noalloc_matches_sgemm_on_two_calls(lib, math_mode, M, N, K, kind):
     import torch
     A_h = matgen.KINDS[kind](17, matgen.MATRIX_A, M, K)
     B_h = matgen.KINDS[kind](17, matgen.MATRIX_B, K, N)
