@@ -55,6 +55,8 @@ def algorithmic_bytes(M, N, K):
 KERNEL_SOURCES = {
     "k_tiled_tma": ["sgemm_tiled.cu", "ptx.cuh", "kernels.h"],
     "k_tf32x3": ["sgemm_tf32x3.cu", "tcgen05.cuh", "ptx.cuh", "kernels.h"],
+    "k_tf32x3_pair": ["sgemm_tf32x3.cu", "tcgen05.cuh", "ptx.cuh",
+                      "kernels.h"],
 }
 
 
@@ -369,8 +371,9 @@ def run_gpu(args, w):
                   "clock sampled during the timed region)"
                   % (sms, FMA_PER_CLK_PER_SM, peak_clock_mhz))
     kernel = {"tiled_tma": "k_tiled_tma", "tiled_ldg": "k_tiled_ldg",
-              "tf32x3": "k_tf32x3"}.get(plan, plan)
-    if plan == "tf32x3":
+              "tf32x3": "k_tf32x3", "tf32x3_pair": "k_tf32x3_pair"}.get(
+                  plan, plan)
+    if plan.startswith("tf32x3"):
         bf16, src = measured_bf16_tflops()
         tf32_peak = bf16 * TF32_PER_BF16
         eff_peak = tf32_peak / TF32X3_PRODUCTS
@@ -394,7 +397,7 @@ def run_gpu(args, w):
 
     # The CUDA-core FFMA kernel on the same inputs, timed the same way.
     ffma = None
-    if plan == "tf32x3" and not args.no_ffma:
+    if plan.startswith("tf32x3") and not args.no_ffma:
         prev = dfm.sgemm_set_math_mode("ffma")
         try:
             ffma_path = dfm.sgemm_plan(M, N, K, K, N, N, A.data_ptr(),
@@ -417,7 +420,7 @@ def run_gpu(args, w):
         "config": config_of(w, extra={
             "path": plan, "sms": sms, "gpu": props.name,
             "arithmetic": ("3xTF32 tensor-core products (hi/lo split), fp32 "
-                           "accumulation" if plan == "tf32x3" else
+                           "accumulation" if plan.startswith("tf32x3") else
                            "fp32 fused multiply-add on CUDA cores"),
             "l2": "flushed before every step (256 MiB device memset, "
                   "outside the timed events)",

@@ -88,6 +88,11 @@ cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
 cudaError_t tf32x3_init();
 cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
                           const CUtensorMap& tmB, int* status, cudaStream_t s);
+// 2-SM variant: 256 x 256 tiles, clusters of 2 blocks (same maps: each block
+// loads A boxes {32, 128} and B boxes {32, 32}).
+cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
+                               const CUtensorMap& tmB, int* status,
+                               cudaStream_t s);
 
 // M == 1 and N == 1 bandwidth kernels for any layout; one-thread-per-output
 // kernel.

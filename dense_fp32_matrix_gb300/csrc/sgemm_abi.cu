@@ -25,6 +25,8 @@ std::atomic<int> g_math_mode{SGEMM_MATH_AUTO};
 // kernel (which splits K over all SMs) beats one tensor-core block per tile.
 constexpr int64_t kTf32MinTiles = 64;
 constexpr int64_t kTf32LongK = 2048;
+// From this many 256 x 256 tiles on, the 2-SM pair kernel beats the 1-SM one.
+constexpr int64_t kTf32PairMinTiles = 32;
 // Largest M, N or K the int-indexed kernels accept (tile rounding included).
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1024;
 
@@ -181,8 +183,11 @@ int plan_path(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
     const int64_t tiles = ((M + kTileM - 1) / kTileM) *
                           ((N + kTileN - 1) / kTileN);
     if (g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO &&
-        !(tiles < kTf32MinTiles && K >= kTf32LongK))
-      return SGEMM_PATH_TF32X3;
+        !(tiles < kTf32MinTiles && K >= kTf32LongK)) {
+      const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+      return pair_tiles >= kTf32PairMinTiles ? SGEMM_PATH_TF32X3_PAIR
+                                             : SGEMM_PATH_TF32X3;
+    }
     return SGEMM_PATH_TILED_TMA;
   }
   return SGEMM_PATH_TILED_LDG;
@@ -297,7 +302,8 @@ int to_status(cudaError_t e) {
              : SGEMM_ERR_CUDA;
 }
 
-int run_tf32x3(const GemmArgs& g, const DeviceState& st, cudaStream_t s) {
+int run_tf32x3(const GemmArgs& g, const DeviceState& st, cudaStream_t s,
+               bool pair) {
   CUtensorMap tmA, tmB;
   int rc = encode_2d(&tmA, g.A, g.K, g.M, g.lda, 32, 128,
                      CU_TENSOR_MAP_SWIZZLE_128B);
@@ -305,7 +311,8 @@ int run_tf32x3(const GemmArgs& g, const DeviceState& st, cudaStream_t s) {
     rc = encode_2d(&tmB, g.B, g.N, g.K, g.ldb, 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != SGEMM_OK) return rc;
-  return to_status(launch_tf32x3(g, tmA, tmB, st.status, s));
+  return to_status(pair ? launch_tf32x3_pair(g, tmA, tmB, st.status, s)
+                        : launch_tf32x3(g, tmA, tmB, st.status, s));
 }
 
 int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
@@ -364,9 +371,10 @@ int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
     case SGEMM_PATH_NAIVE:
       return to_status(launch_naive(g, s));
     case SGEMM_PATH_TF32X3:
+    case SGEMM_PATH_TF32X3_PAIR:
       if (!tma_operand_ok(a, lda) || !tma_operand_ok(b, ldb))
         return SGEMM_ERR_PATH;
-      return run_tf32x3(g, *st, s);
+      return run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR);
     default:
       return SGEMM_ERR_PATH;
   }
@@ -415,7 +423,8 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
     case SGEMM_PATH_TF32X3:
-      return run_tf32x3(g, *st, s);
+    case SGEMM_PATH_TF32X3_PAIR:
+      return run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR);
     case SGEMM_PATH_GEMV_ROW: {
       const cudaError_t e = run_gemv_row(g, *st, s, &rc);
       return rc != SGEMM_OK ? rc : to_status(e);
@@ -552,6 +561,7 @@ const char* sgemm_path_name(int path) {
     case SGEMM_PATH_GEMV_COL: return "gemv_col";
     case SGEMM_PATH_NAIVE: return "naive";
     case SGEMM_PATH_TF32X3: return "tf32x3";
+    case SGEMM_PATH_TF32X3_PAIR: return "tf32x3_pair";
     default: return "?";
   }
 }

@@ -282,12 +282,227 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
+// ---------------------------------------------------------------- pairs
+//
+// 2-SM variant: a cluster of two blocks computes a 256 x 256 tile with the
+// pair MMA (M = 256, N = 256, K = 8). Block r of the pair holds rows
+// 128 r .. 128 r + 127 of A's slice and columns 128 r .. 128 r + 127 of B's,
+// in the same 64 KiB stage layout as above; every operand byte is read from
+// shared memory once for both tensor cores, which halves the operand reads
+// per flop. The split warps of both blocks arrive on the even block's split
+// barrier (cluster scope); that block's thread 32 issues the MMAs and commits
+// each stage's release and the final accumulator to both blocks. Each block
+// stores its own 128 x 256 rows from its tensor memory.
+constexpr int PM = 256, PN = 256;
+constexpr int P_TMEM_COLS = 256;
+constexpr int P_CONV_ARRIVALS = 2 * (X_CONV_THREADS / 32);
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile(
+      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+          cluster_addr)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(X_THREADS, 1)
+k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
+              const __grid_constant__ CUtensorMap tmB, float* __restrict__ C,
+              int M, int N, int K, long long ldc, int tiles_m, int tiles_n,
+              int vec_store, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* ctrl = smem + XSTAGES * X_STAGE;
+  const uint32_t full0 = smem_u32(ctrl);          // own TMA landed
+  const uint32_t conv0 = full0 + 8 * XSTAGES;     // both blocks split (even)
+  const uint32_t empty0 = conv0 + 8 * XSTAGES;    // pair MMAs done reading
+  const uint32_t accf = empty0 + 8 * XSTAGES;     // accumulator complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (3 * XSTAGES + 1));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto A_of = [&](int s) { return smem + s * X_STAGE; };
+  auto Alo_of = [&](int s) { return smem + s * X_STAGE + X_A_BYTES; };
+  auto B_of = [&](int s) { return smem + s * X_STAGE + 2 * X_A_BYTES; };
+  auto Blo_of = [&](int s) {
+    return smem + s * X_STAGE + 2 * X_A_BYTES + X_B_BYTES;
+  };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  int pm, pn;
+  tile_of(blockIdx.x >> 1, tiles_m, tiles_n, pm, pn);
+  const int m_own = pm * PM + 128 * int(rank);  // this block's rows
+  const int n_pair = pn * PN;                   // the pair's columns
+  const int n_own = n_pair + 128 * int(rank);   // this block's B columns
+  const int T = (K + XK - 1) / XK;
+
+  if (tid == 0) {
+    for (int s = 0; s < XSTAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(conv0 + 8 * s, P_CONV_ARRIVALS);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(accf, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc_pair(smem_u32(tmem_slot), P_TMEM_COLS);
+    tc::tmem_relinquish_pair();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();  // both blocks' barriers exist before any remote use
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int t = 0; t < T && !*abort_flag; ++t) {
+        const int s = t % XSTAGES;
+        if (t >= XSTAGES &&
+            !mbar_wait_bounded(empty0 + 8 * s, ((t / XSTAGES) - 1) & 1, status,
+                               kSiteTf32Empty, kWaitLimitNs)) {
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t bar = full0 + 8 * s;
+        mbar_arrive_expect_tx(bar, X_A_BYTES + X_B_BYTES);
+        tma_load_2d(smem_u32(A_of(s)), &tmA, t * XK, m_own, bar);
+        for (int j = 0; j < 128 / 32; ++j)
+          tma_load_2d(smem_u32(B_of(s) + j * X_B_BOX), &tmB, n_own + 32 * j,
+                      t * XK, bar);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = tc::idesc_tf32(PM, PN, false, false);
+      for (int t = 0; t < T; ++t) {
+        const int s = t % XSTAGES;
+        if (*abort_flag ||
+            !mbar_wait_bounded(conv0 + 8 * s, (t / XSTAGES) & 1, status,
+                               kSiteTf32Conv, kWaitLimitNs)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t a = smem_u32(A_of(s)), al = smem_u32(Alo_of(s));
+        const uint32_t b = smem_u32(B_of(s)), bl = smem_u32(Blo_of(s));
+#pragma unroll
+        for (int ks = 0; ks < XK / 8; ++ks) {
+          const uint64_t da = tc::smem_desc(a + 32 * ks, 16, 1024,
+                                            tc::kLayoutSwizzle128);
+          const uint64_t dal = tc::smem_desc(al + 32 * ks, 16, 1024,
+                                             tc::kLayoutSwizzle128);
+          const uint64_t db = tc::smem_desc(b + 32 * ks, 16, 1024,
+                                            tc::kLayoutSwizzle128);
+          const uint64_t dbl = tc::smem_desc(bl + 32 * ks, 16, 1024,
+                                             tc::kLayoutSwizzle128);
+          tc::mma_tf32_pair(tmem, dal, db, idesc, (t > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_tf32_pair(tmem, da, dbl, idesc, 1u);
+          tc::mma_tf32_pair(tmem, da, db, idesc, 1u);
+        }
+        tc::commit_pair_multicast(empty0 + 8 * s, 0x3);
+      }
+      tc::commit_pair_multicast(accf, 0x3);
+    }
+  } else {
+    // ---------------------------------------------------------- split
+    const int ct = tid - 64;  // 0..127
+    const uint32_t conv_leader = cluster_map(conv0, 0);
+    for (int t = 0; t < T; ++t) {
+      const int s = t % XSTAGES;
+      if (*abort_flag ||
+          !mbar_wait_bounded(full0 + 8 * s, (t / XSTAGES) & 1, status,
+                             kSiteTf32Full, kWaitLimitNs)) {
+        *abort_flag = 1;
+        break;
+      }
+#pragma unroll
+      for (int q = 0; q < X_A_BYTES / 16 / X_CONV_THREADS; ++q)
+        split4(A_of(s), Alo_of(s), ct + X_CONV_THREADS * q);
+      split_transpose_box(B_of(s) + (warp - 2) * X_B_BOX,
+                          Blo_of(s) + (warp - 2) * X_B_BOX, lane);
+      fence_async_shared();  // generic writes -> visible to the MMA
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(conv_leader + 8 * s);
+    }
+    // ---------------------------------------------------------- epilogue
+    const bool ok = mbar_wait_bounded(accf, 0, status, kSiteTf32Acc,
+                                      *abort_flag ? kWaitLimitNs / 100
+                                                  : kWaitLimitNs);
+    tc::fence_after_sync();
+    const int quarter = warp & 3;
+    const int r = m_own + 32 * quarter + lane;
+    float* crow = C + (long long)r * ldc;
+#pragma unroll 1
+    for (int cb = 0; cb < PN / 32; ++cb) {
+      uint32_t v[32];
+      tc::tmem_ld_32x32b_x32(tmem + (uint32_t(32 * quarter) << 16) + 32 * cb,
+                             v);
+      tc::tmem_ld_wait();
+      if (!ok || *abort_flag || r >= M) continue;
+      const int c0 = n_pair + 32 * cb;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const int c = c0 + e;
+        if (vec_store && c + 3 < N) {
+          *reinterpret_cast<float4*>(crow + c) =
+              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                          __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (c + u < N) crow[c + u] = __uint_as_float(v[e + u]);
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();  // the pair's MMAs and both blocks' reads are done
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc_pair(tmem, P_TMEM_COLS);
+  }
+}
+
 }  // namespace
 
 cudaError_t tf32x3_init() {
-  return cudaFuncSetAttribute(k_tf32x3,
+  const cudaError_t e = cudaFuncSetAttribute(
+      k_tf32x3, cudaFuncAttributeMaxDynamicSharedMemorySize, int(X_SMEM));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_tf32x3_pair,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(X_SMEM));
+}
+
+cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
+                               const CUtensorMap& tmB, int* status,
+                               cudaStream_t s) {
+  const int tiles_m = int((g.M + PM - 1) / PM);
+  const int tiles_n = int((g.N + PN - 1) / PN);
+  const bool vec = (g.ldc % 4 == 0) &&
+                   (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2u * unsigned(tiles_m) * unsigned(tiles_n), 1, 1);
+  cfg.blockDim = dim3(X_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = X_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_tf32x3_pair, tmA, tmB, g.C, int(g.M),
+                            int(g.N), int(g.K), (long long)g.ldc, tiles_m,
+                            tiles_n, vec ? 1 : 0, status);
 }
 
 cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,

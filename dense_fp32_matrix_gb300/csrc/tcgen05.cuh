@@ -66,6 +66,30 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
       : "memory");
 }
 
+// Pair (cta_group::2) variants: one warp in each CTA of the 2-CTA cluster
+// allocates / frees the same columns in both tensor memories.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem,
+                                                uint32_t cols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+          dst_smem),
+      "r"(cols)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr,
+                                                  uint32_t cols) {
+  asm volatile(
+      "tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+      "r"(cols)
+      : "memory");
+}
+
 __device__ __forceinline__ void fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -87,6 +111,33 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc,
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Pair MMA issued by the even CTA of a 2-CTA cluster: M = 256 rows, A rows
+// 0..127 from this CTA's shared memory and 128..255 from the peer's at the
+// same offsets, B columns split the same way; D lands in both tensor
+// memories (each CTA holds its 128 rows x N).
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc,
+                                             uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once, in every CTA of `cta_mask`, on the mbarrier at this shared
+// offset when the pair's tcgen05 operations issued so far have completed.
+__device__ __forceinline__ void commit_pair_multicast(uint32_t mbar,
+                                                      uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;" ::"r"(mbar),
+      "h"(cta_mask)
       : "memory");
 }
 

@@ -90,7 +90,8 @@ extern "C" {
 #define SGEMM_PATH_GEMV_COL 4   /* N == 1: c = A * b, one warp per row     */
 #define SGEMM_PATH_NAIVE 5      /* one thread per output (debug baseline)  */
 #define SGEMM_PATH_TF32X3 6     /* tensor cores, 3 TF32 products (aligned)  */
-#define SGEMM_PATH_COUNT 7
+#define SGEMM_PATH_TF32X3_PAIR 7 /* same on 2-SM pairs, 256 x 256 tiles     */
+#define SGEMM_PATH_COUNT 8
 
 /*
  * sgemm: C = A * B as described above, on `stream`.

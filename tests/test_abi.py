@@ -63,13 +63,15 @@ C16 = 0x7f0020000000
 
 
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc,a,b,expect", [
-    (4096, 4096, 4096, 4096, 4096, 4096, A16, B16, "tf32x3"),
+    (4096, 4096, 4096, 4096, 4096, 4096, A16, B16, "tf32x3_pair"),
     (256, 256, 256, 256, 256, 256, A16, B16, "tf32x3"),
+    (1024, 1024, 1024, 1024, 1024, 1024, A16, B16, "tf32x3"),
+    (2048, 2048, 2048, 2048, 2048, 2048, A16, B16, "tf32x3_pair"),
     (512, 512, 4096, 4096, 512, 512, A16, B16, "tiled_tma"),  # few tiles, long K
     (4095, 4097, 1023, 1023, 4097, 4097, A16, B16, "tiled_ldg"),  # ld % 4
     (127, 129, 33, 33, 129, 129, A16, B16, "tiled_ldg"),
     (4096, 4096, 4096, 4096, 4096, 4096, A16 + 4, B16, "tiled_ldg"),  # align
-    (4096, 4096, 4096, 4100, 4096, 4096, A16, B16, "tf32x3"),  # pitch
+    (4096, 4096, 4096, 4100, 4096, 4096, A16, B16, "tf32x3_pair"),  # pitch
     (1, 4096, 4096, 4096, 4096, 4096, A16, B16, "gemv_row"),
     (4096, 1, 4096, 4096, 1, 1, A16, B16, "gemv_col"),
     (1, 1, 7, 7, 1, 1, A16, B16, "gemv_row"),
@@ -88,7 +90,7 @@ def test_math_mode_restricts_to_cuda_cores(lib):
     finally:
         assert dfm.sgemm_set_math_mode("auto") == "ffma"
     assert dfm.sgemm_plan(4096, 4096, 4096, 4096, 4096, 4096, A16, B16,
-                          C16) == "tf32x3"
+                          C16) == "tf32x3_pair"
     with pytest.raises(dfm.SgemmError):
         dfm.sgemm_set_math_mode(7)
 

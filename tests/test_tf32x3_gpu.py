@@ -15,7 +15,8 @@ from gpu_util import run_case
 
 pytestmark = pytest.mark.gpu
 
-PATH = "tf32x3"
+PATH = "tf32x3"          # one block per 128 x 128 tile
+PAIR = "tf32x3_pair"     # 2-SM clusters, 256 x 256 tiles
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -27,9 +28,10 @@ def _lib():
 ALIGNED = [w for w in WORKLOADS if w["K"] % 4 == 0 and w["N"] % 4 == 0]
 
 
+@pytest.mark.parametrize("path", [PATH, PAIR])
 @pytest.mark.parametrize("w", ALIGNED, ids=lambda w: w["name"])
-def test_workload(w):
-    worst = run_case(w["M"], w["N"], w["K"], w["kind"], w["seed"], path=PATH)
+def test_workload(w, path):
+    worst = run_case(w["M"], w["N"], w["K"], w["kind"], w["seed"], path=path)
     if w["kind"] != "integers":
         # the split's extra error is ~3 * 2^-20 of each |product|
         assert worst < 0.25
@@ -40,20 +42,23 @@ def test_workload(w):
                                  (384, 256, 24), (1, 4096, 256), (4096, 4, 64)],
                          ids=str)
 @pytest.mark.parametrize("kind", ["uniform", "integers", "normal"])
-def test_multi_tile(mnk, kind):
-    run_case(*mnk, kind=kind, seed=sum(mnk), path=PATH)
+@pytest.mark.parametrize("path", [PATH, PAIR])
+def test_multi_tile(mnk, kind, path):
+    run_case(*mnk, kind=kind, seed=sum(mnk), path=path)
 
 
-def test_tiny_aligned_shapes_bit_exact():
+@pytest.mark.parametrize("path", [PATH, PAIR])
+def test_tiny_aligned_shapes_bit_exact(path):
     for M, N, K in itertools.product((1, 2, 3, 5, 8, 17, 33, 129),
                                      (4, 8, 12, 36, 132), (4, 8, 12, 36, 68)):
-        run_case(M, N, K, kind="integers", seed=M * 7 + N * 3 + K, path=PATH,
+        run_case(M, N, K, kind="integers", seed=M * 7 + N * 3 + K, path=path,
                  check="full")
 
 
-def test_pitch_padding_never_read_or_written():
-    run_case(300, 200, 64, "uniform", 9, lda=72, ldb=204, ldc=260, path=PATH)
-    run_case(260, 132, 36, "integers", 9, lda=40, ldb=136, ldc=133, path=PATH)
+@pytest.mark.parametrize("path", [PATH, PAIR])
+def test_pitch_padding_never_read_or_written(path):
+    run_case(300, 200, 64, "uniform", 9, lda=72, ldb=204, ldc=260, path=path)
+    run_case(260, 132, 36, "integers", 9, lda=40, ldb=136, ldc=133, path=path)
 
 
 def test_unaligned_layout_is_refused():
@@ -100,14 +105,18 @@ def test_auto_dispatch_picks_the_tensor_path_for_aligned_operands():
     assert dfm.sgemm_plan(640, 260, 388, 388, 260, 260, A.data_ptr(),
                           B.data_ptr(), 0x7f0020000000) == PATH
     run_case(640, 260, 388, "integers", 3, path="auto")
+    assert dfm.sgemm_plan(2048, 2048, 260, 260, 2048, 2048, A.data_ptr(),
+                          B.data_ptr(), 0x7f0020000000) == PAIR
+    run_case(2048, 2048, 260, "integers", 3, path="auto")
 
 
-def test_deterministic():
+@pytest.mark.parametrize("path", [PATH, PAIR])
+def test_deterministic(path):
     import torch
     import dense_fp32_matrix_gb300 as dfm
     A = torch.from_numpy(matgen.uniform(2, 0, 1000, 780)).cuda()
     B = torch.from_numpy(matgen.uniform(2, 1, 780, 996)).cuda()
-    C1 = dfm.matmul(A, B, path=PATH)
-    C2 = dfm.matmul(A, B, path=PATH)
+    C1 = dfm.matmul(A, B, path=path)
+    C2 = dfm.matmul(A, B, path=path)
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
