@@ -31,6 +31,7 @@ enum WaitSite : int {
   kSiteTf32Conv = 7,
   kSiteTf32Empty = 8,
   kSiteTf32Acc = 9,
+  kSiteTf32Peer = 10,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -74,28 +75,43 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar,
       : "memory");
 }
 
+// kCluster: acquire at cluster scope, for a barrier that blocks of the
+// cluster arrive on with release.cluster (their writes become visible).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (kCluster) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], "
+        "%2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
 // Wait until phase `parity` of the mbarrier completes, for at most
 // `limit_ns` nanoseconds (and at most 2^31 polls as a second bound). Returns
 // false on timeout after recording it.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   int* status, int site,
                                                   uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1; it < (1u << 31); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if ((it & 15u) == 0 && global_timer_ns() - t0 > limit_ns) break;
   }
   record_timeout(status, site);

@@ -289,13 +289,15 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
 // 128 r .. 128 r + 127 of A's slice and columns 128 r .. 128 r + 127 of B's,
 // in the same 64 KiB stage layout as above; every operand byte is read from
 // shared memory once for both tensor cores, which halves the operand reads
-// per flop. The split warps of both blocks arrive on the even block's split
-// barrier (cluster scope); that block's thread 32 issues the MMAs and commits
+// per flop. The split warps of each block arrive on their own block's split
+// barrier; in the odd block one thread of warp 1 waits for that barrier and
+// forwards a single cluster-scope release arrival to the even block's peer
+// barrier (one cluster-scope fence per stage instead of one per split warp).
+// The even block's thread 32 waits for both, issues the MMAs and commits
 // each stage's release and the final accumulator to both blocks. Each block
 // stores its own 128 x 256 rows from its tensor memory.
 constexpr int PM = 256, PN = 256;
 constexpr int P_TMEM_COLS = 256;
-constexpr int P_CONV_ARRIVALS = 2 * (X_CONV_THREADS / 32);
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile(
@@ -314,10 +316,11 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* ctrl = smem + XSTAGES * X_STAGE;
   const uint32_t full0 = smem_u32(ctrl);          // own TMA landed
-  const uint32_t conv0 = full0 + 8 * XSTAGES;     // both blocks split (even)
+  const uint32_t conv0 = full0 + 8 * XSTAGES;     // own split done
   const uint32_t empty0 = conv0 + 8 * XSTAGES;    // pair MMAs done reading
-  const uint32_t accf = empty0 + 8 * XSTAGES;     // accumulator complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (3 * XSTAGES + 1));
+  const uint32_t peer0 = empty0 + 8 * XSTAGES;    // odd block split (even)
+  const uint32_t accf = peer0 + 8 * XSTAGES;      // accumulator complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (4 * XSTAGES + 1));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto A_of = [&](int s) { return smem + s * X_STAGE; };
   auto Alo_of = [&](int s) { return smem + s * X_STAGE + X_A_BYTES; };
@@ -338,8 +341,9 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
   if (tid == 0) {
     for (int s = 0; s < XSTAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(conv0 + 8 * s, P_CONV_ARRIVALS);
+      mbar_init(conv0 + 8 * s, X_CONV_THREADS / 32);
       mbar_init(empty0 + 8 * s, 1);
+      mbar_init(peer0 + 8 * s, 1);
     }
     mbar_init(accf, 1);
     *abort_flag = 0;
@@ -382,9 +386,12 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       constexpr uint32_t idesc = tc::idesc_tf32(PM, PN, false, false);
       for (int t = 0; t < T; ++t) {
         const int s = t % XSTAGES;
+        const uint32_t par = (t / XSTAGES) & 1;
         if (*abort_flag ||
-            !mbar_wait_bounded(conv0 + 8 * s, (t / XSTAGES) & 1, status,
-                               kSiteTf32Conv, kWaitLimitNs)) {
+            !mbar_wait_bounded(conv0 + 8 * s, par, status, kSiteTf32Conv,
+                               kWaitLimitNs) ||
+            !mbar_wait_bounded<true>(peer0 + 8 * s, par, status,
+                                     kSiteTf32Peer, kWaitLimitNs)) {
           *abort_flag = 1;
           break;
         }
@@ -408,11 +415,25 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
         tc::commit_pair_multicast(empty0 + 8 * s, 0x3);
       }
       tc::commit_pair_multicast(accf, 0x3);
+    } else if (lane == 0) {
+      // odd block: forward each completed split to the even block. The
+      // acquire of the local wait and the cumulative cluster-scope release
+      // order all four split warps' writes before the even block's MMAs.
+      const uint32_t peer_leader = cluster_map(peer0, 0);
+      for (int t = 0; t < T; ++t) {
+        const int s = t % XSTAGES;
+        if (*abort_flag ||
+            !mbar_wait_bounded(conv0 + 8 * s, (t / XSTAGES) & 1, status,
+                               kSiteTf32Conv, kWaitLimitNs)) {
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_cluster(peer_leader + 8 * s);
+      }
     }
   } else {
     // ---------------------------------------------------------- split
     const int ct = tid - 64;  // 0..127
-    const uint32_t conv_leader = cluster_map(conv0, 0);
     for (int t = 0; t < T; ++t) {
       const int s = t % XSTAGES;
       if (*abort_flag ||
@@ -428,7 +449,7 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
                           Blo_of(s) + (warp - 2) * X_B_BOX, lane);
       fence_async_shared();  // generic writes -> visible to the MMA
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(conv_leader + 8 * s);
+      if (lane == 0) mbar_arrive(conv0 + 8 * s);
     }
     // ---------------------------------------------------------- epilogue
     const bool ok = mbar_wait_bounded(accf, 0, status, kSiteTf32Acc,
