@@ -85,13 +85,33 @@ cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
 // 3xTF32 tensor-core kernel (sgemm_tf32x3.cu). tmA: A as dims {K, M}, box
 // {32, 128}, 128-byte swizzle; tmB: B as dims {N, K}, box {32, 32}, 128-byte
 // swizzle. Needs 16-byte aligned bases and row strides.
-cudaError_t tf32x3_init();
+// tf32x3_init also reports how many 2-block clusters of the pair kernel fit
+// on the device at once.
+cudaError_t tf32x3_init(int* pair_clusters);
 cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
                           const CUtensorMap& tmB, int* status, cudaStream_t s);
-// 2-SM variant: 256 x 256 tiles, clusters of 2 blocks (same maps: each block
-// loads A boxes {32, 128} and B boxes {32, 32}).
+
+// 2-SM variant: 256 x 256 tiles, persistent clusters of 2 blocks with a
+// stream-K tail (same maps: each block loads A boxes {32, 128} and B boxes
+// {32, 32}).
+struct PairPlan {
+  int tiles_m, tiles_n, tiles;
+  int T;              // k-slices of 32 per tile
+  int G;              // clusters launched
+  int dp_tiles;       // tiles computed whole
+  int sk_tiles;       // tiles split by k-slices over all clusters
+  int64_t sk_iters;   // sk_tiles * T
+  size_t ws_floats;   // partial-tile workspace (0 without stream-K)
+  size_t counters;    // tile counters (zero before the launch)
+};
+// Stream-K shares shorter than this many k-slices are not worth their
+// fix-up; the schedule widens the split part by a wave instead.
+constexpr int kPairMinSkIters = 8;
+PairPlan plan_pair(int64_t M, int64_t N, int64_t K, int clusters,
+                   bool stream_k);
 cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
-                               const CUtensorMap& tmB, int* status,
+                               const CUtensorMap& tmB, const PairPlan& pl,
+                               float* ws, int* counters, int* status,
                                cudaStream_t s);
 
 // M == 1 and N == 1 bandwidth kernels for any layout; one-thread-per-output

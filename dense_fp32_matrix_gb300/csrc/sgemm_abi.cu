@@ -8,6 +8,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <unordered_map>
 
 #include "dfm_sgemm.h"
 #include "kernels.h"
@@ -30,18 +31,25 @@ constexpr int64_t kTf32PairMinTiles = 32;
 // Largest M, N or K the int-indexed kernels accept (tile rounding included).
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1024;
 
+struct Workspace {
+  float* ws = nullptr;
+  size_t ws_floats = 0;
+  int* counters = nullptr;
+  size_t counters_len = 0;
+};
+
 struct DeviceState {
   std::once_flag once;
   int err = SGEMM_OK;
   int sms = 0;
   int tma_blocks_per_sm = 0;
+  int pair_clusters = 0;  // 2-block clusters of the pair kernel at once
   int* status = nullptr;
-  // Stream-K workspace of the TMA path: partial tiles, then tile counters.
+  // Stream-K workspaces (partial tiles and tile counters), one per stream
+  // the library has been called on: kernels on unordered streams may run
+  // at the same time, so they must not share partial tiles or counters.
   std::mutex ws_mu;
-  float* ws = nullptr;
-  size_t ws_floats = 0;
-  int* counters = nullptr;
-  size_t counters_len = 0;
+  std::unordered_map<cudaStream_t, Workspace> ws;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -92,7 +100,8 @@ void init_device(DeviceState& st) {
       cudaMemset(st.status, 0, sizeof(int) * 4) != cudaSuccess ||
       tiled_init(&st.tma_blocks_per_sm) != cudaSuccess ||
       st.tma_blocks_per_sm < 1 || small_init() != cudaSuccess ||
-      gemv_tma_init() != cudaSuccess || tf32x3_init() != cudaSuccess) {
+      gemv_tma_init() != cudaSuccess ||
+      tf32x3_init(&st.pair_clusters) != cudaSuccess) {
     st.err = SGEMM_ERR_CUDA;
     return;
   }
@@ -110,28 +119,31 @@ int device_state(DeviceState** out) {
   return st.err;
 }
 
-// Make the device's stream-K workspace at least `floats` partial-tile
-// floats and `tiles` counters. Growing frees the old buffers (cudaFree waits
-// for the device) and zeroes the new counters.
-int ensure_workspace(DeviceState& st, size_t floats, size_t tiles) {
-  std::lock_guard<std::mutex> lock(st.ws_mu);
-  if (floats > st.ws_floats) {
-    if (st.ws != nullptr) cudaFree(st.ws);
-    st.ws = nullptr;
-    st.ws_floats = 0;
-    if (cudaMalloc(&st.ws, floats * sizeof(float)) != cudaSuccess)
+// Make the workspace of stream s at least `floats` partial-tile floats and
+// `counters` tile counters; the caller holds st.ws_mu until its launch is
+// enqueued. Growing frees the old buffers (cudaFree waits for the device, so
+// kernels still using them finish first) and zeroes the new counters.
+int ensure_workspace(DeviceState& st, cudaStream_t s, size_t floats,
+                     size_t counters, Workspace** out) {
+  Workspace& w = st.ws[s];
+  if (floats > w.ws_floats) {
+    if (w.ws != nullptr) cudaFree(w.ws);
+    w.ws = nullptr;
+    w.ws_floats = 0;
+    if (cudaMalloc(&w.ws, floats * sizeof(float)) != cudaSuccess)
       return SGEMM_ERR_CUDA;
-    st.ws_floats = floats;
+    w.ws_floats = floats;
   }
-  if (tiles > st.counters_len) {
-    if (st.counters != nullptr) cudaFree(st.counters);
-    st.counters = nullptr;
-    st.counters_len = 0;
-    if (cudaMalloc(&st.counters, tiles * sizeof(int)) != cudaSuccess ||
-        cudaMemset(st.counters, 0, tiles * sizeof(int)) != cudaSuccess)
+  if (counters > w.counters_len) {
+    if (w.counters != nullptr) cudaFree(w.counters);
+    w.counters = nullptr;
+    w.counters_len = 0;
+    if (cudaMalloc(&w.counters, counters * sizeof(int)) != cudaSuccess ||
+        cudaMemset(w.counters, 0, counters * sizeof(int)) != cudaSuccess)
       return SGEMM_ERR_CUDA;
-    st.counters_len = tiles;
+    w.counters_len = counters;
   }
+  *out = &w;
   return SGEMM_OK;
 }
 
@@ -302,17 +314,27 @@ int to_status(cudaError_t e) {
              : SGEMM_ERR_CUDA;
 }
 
-int run_tf32x3(const GemmArgs& g, const DeviceState& st, cudaStream_t s,
+int encode_tf32x3(const GemmArgs& g, CUtensorMap* tmA, CUtensorMap* tmB) {
+  const int rc = encode_2d(tmA, g.A, g.K, g.M, g.lda, 32, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != SGEMM_OK) return rc;
+  return encode_2d(tmB, g.B, g.N, g.K, g.ldb, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
                bool pair) {
   CUtensorMap tmA, tmB;
-  int rc = encode_2d(&tmA, g.A, g.K, g.M, g.lda, 32, 128,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc == SGEMM_OK)
-    rc = encode_2d(&tmB, g.B, g.N, g.K, g.ldb, 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
+  const int rc = encode_tf32x3(g, &tmA, &tmB);
   if (rc != SGEMM_OK) return rc;
-  return to_status(pair ? launch_tf32x3_pair(g, tmA, tmB, st.status, s)
-                        : launch_tf32x3(g, tmA, tmB, st.status, s));
+  if (!pair) return to_status(launch_tf32x3(g, tmA, tmB, st.status, s));
+  const PairPlan pl = plan_pair(g.M, g.N, g.K, st.pair_clusters, true);
+  std::lock_guard<std::mutex> lock(st.ws_mu);
+  Workspace* w = nullptr;
+  const int wrc = ensure_workspace(st, s, pl.ws_floats, pl.counters, &w);
+  if (wrc != SGEMM_OK) return wrc;
+  return to_status(launch_tf32x3_pair(g, tmA, tmB, pl, w->ws, w->counters,
+                                      st.status, s));
 }
 
 int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
@@ -351,10 +373,12 @@ int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
       if (rc != SGEMM_OK) return rc;
       const SkPlan pl =
           plan_stream_k(M, N, K, st->sms * st->tma_blocks_per_sm);
-      rc = ensure_workspace(*st, pl.ws_floats, size_t(pl.tiles));
+      std::lock_guard<std::mutex> lock(st->ws_mu);
+      Workspace* w = nullptr;
+      rc = ensure_workspace(*st, s, pl.ws_floats, size_t(pl.tiles), &w);
       if (rc != SGEMM_OK) return rc;
-      return to_status(launch_tiled_tma(g, tmA, tmB, pl, st->ws,
-                                        st->counters, st->status, s));
+      return to_status(launch_tiled_tma(g, tmA, tmB, pl, w->ws, w->counters,
+                                        st->status, s));
     }
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
@@ -423,8 +447,23 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
     case SGEMM_PATH_TF32X3:
-    case SGEMM_PATH_TF32X3_PAIR:
-      return run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR);
+      return run_tf32x3(g, *st, s, false);
+    case SGEMM_PATH_TF32X3_PAIR: {
+      CUtensorMap tmA, tmB;
+      rc = encode_tf32x3(g, &tmA, &tmB);
+      if (rc != SGEMM_OK) return rc;
+      // stream-K tail only when its workspace fits in the scratch
+      PairPlan pl = plan_pair(M, N, K, st->pair_clusters, true);
+      if (pl.ws_floats > ws_floats || pl.counters > counters_len)
+        pl = plan_pair(M, N, K, st->pair_clusters, false);
+      if (pl.counters > 0) {
+        rc = to_status(
+            cudaMemsetAsync(counters, 0, pl.counters * sizeof(int), s));
+        if (rc != SGEMM_OK) return rc;
+      }
+      return to_status(launch_tf32x3_pair(g, tmA, tmB, pl, ws, counters,
+                                          st->status, s));
+    }
     case SGEMM_PATH_GEMV_ROW: {
       const cudaError_t e = run_gemv_row(g, *st, s, &rc);
       return rc != SGEMM_OK ? rc : to_status(e);
@@ -514,10 +553,11 @@ int sgemm_watchdog_status(int* site) {
   // raised; clear them so later calls start from zero.
   {
     std::lock_guard<std::mutex> lock(st->ws_mu);
-    if (st->counters != nullptr &&
-        cudaMemset(st->counters, 0, st->counters_len * sizeof(int)) !=
-            cudaSuccess)
-      return SGEMM_ERR_CUDA;
+    for (auto& kv : st->ws)
+      if (kv.second.counters != nullptr &&
+          cudaMemset(kv.second.counters, 0,
+                     kv.second.counters_len * sizeof(int)) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
   }
   return SGEMM_ERR_WATCHDOG;
 }

@@ -284,20 +284,60 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
 
 // ---------------------------------------------------------------- pairs
 //
-// 2-SM variant: a cluster of two blocks computes a 256 x 256 tile with the
+// 2-SM variant: a cluster of two blocks computes 256 x 256 tiles with the
 // pair MMA (M = 256, N = 256, K = 8). Block r of the pair holds rows
 // 128 r .. 128 r + 127 of A's slice and columns 128 r .. 128 r + 127 of B's,
 // in the same 64 KiB stage layout as above; every operand byte is read from
 // shared memory once for both tensor cores, which halves the operand reads
-// per flop. The split warps of each block arrive on their own block's split
-// barrier; in the odd block one thread of warp 1 waits for that barrier and
-// forwards a single cluster-scope release arrival to the even block's peer
-// barrier (one cluster-scope fence per stage instead of one per split warp).
-// The even block's thread 32 waits for both, issues the MMAs and commits
-// each stage's release and the final accumulator to both blocks. Each block
-// stores its own 128 x 256 rows from its tensor memory.
+// per flop.
+//
+// Persistent, with a stream-K tail: the grid is the G clusters that fit on
+// the GPU at once. Whole tiles are dealt round-robin in full waves (tile
+// c + i G to cluster c); the k-slices of the remaining tiles (fewer than one
+// wave, or one wave more when that share would be short) are split evenly
+// over all G clusters, so no partly filled last wave is left. A cluster's
+// share is a run of k-ranges ("units"); a unit that covers its whole tile
+// stores C directly, a partial one writes its fp32 piece to the workspace
+// and the last of the tile's pieces to arrive adds them all in k order and
+// stores C (no cluster waits on another; the sum order is fixed).
+//
+// Roles in each block (320 threads):
+//   warp 0      TMA producer over the cluster's units, one ring of stages;
+//   warp 1      even block: allocates 512 tensor-memory columns (two
+//               256-column accumulators) for both blocks and issues the
+//               MMAs; odd block: forwards each completed split to the even
+//               block with one cluster-scope release (one fence per stage
+//               rather than one per split warp);
+//   warps 2..5  split and transpose each landed stage (as above) and arrive
+//               on their own block's split barrier;
+//   warps 6..9  epilogue, one tensor-memory lane quarter each: read a
+//               finished accumulator, store C or the piece, hand the
+//               accumulator back. With two accumulators the MMAs of the
+//               next unit run while the previous one is stored.
 constexpr int PM = 256, PN = 256;
-constexpr int P_TMEM_COLS = 256;
+constexpr int P_THREADS = 320;
+constexpr int P_ACC_COLS = 256;                      // one accumulator
+constexpr int P_TMEM_COLS = 2 * P_ACC_COLS;
+constexpr int P_EPI_WARP0 = 6;
+constexpr int P_EPI_ARRIVALS = 2 * 4;                // 4 warps x 2 blocks
+constexpr int P_PIECE_FLOATS = 128 * PN;             // one block's half tile
+constexpr size_t P_SMEM = size_t(XSTAGES) * X_STAGE + 1024 + 256;
+
+struct PairParams {
+  float* C;
+  int M, N, K;
+  long long ldc;
+  int tiles_m, tiles_n;
+  int T;                // k-slices per tile
+  int G;                // clusters
+  int dp_tiles;         // tiles dealt whole, a multiple of G (or all tiles)
+  int sk_tiles;         // tiles after them, split by k-slices
+  long long sk_iters;   // sk_tiles * T
+  float* ws;            // 2 pieces per block: G x 2 x 2 x P_PIECE_FLOATS
+  int* counters;        // sk_tiles x 2 blocks x 4 quarters, zero between calls
+  int vec_store;
+  int* status;
+};
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile(
@@ -306,11 +346,78 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
       : "memory");
 }
 
-__global__ void __launch_bounds__(X_THREADS, 1)
+__device__ __forceinline__ long long sk_begin(int c, const PairParams& p) {
+  return (long long)c * p.sk_iters / p.G;
+}
+
+// The cluster whose stream-K share holds iteration x: the largest c with
+// sk_begin(c) <= x.
+__device__ __forceinline__ int sk_owner(long long x, const PairParams& p) {
+  return int(((x + 1) * p.G + p.sk_iters - 1) / p.sk_iters) - 1;
+}
+
+struct Unit {
+  int tile;    // output tile (grouped raster order)
+  int kb, ke;  // k-slices [kb, ke)
+  int sk;      // stream-K tile index when the unit is a partial piece, else -1
+};
+
+// Unit u of cluster c; false past the cluster's last unit.
+__device__ __forceinline__ bool unit_of(int c, int u, const PairParams& p,
+                                        Unit& w) {
+  const int dp_units = c < p.dp_tiles ? (p.dp_tiles - c + p.G - 1) / p.G : 0;
+  if (u < dp_units) {
+    w.tile = c + u * p.G;
+    w.kb = 0;
+    w.ke = p.T;
+    w.sk = -1;
+    return true;
+  }
+  if (p.sk_tiles == 0) return false;
+  const long long b = sk_begin(c, p), e = sk_begin(c + 1, p);
+  const int v = u - dp_units;
+  const long long x = v == 0 ? b : (b / p.T + v) * p.T;
+  if (x >= e) return false;
+  const int tau = int(x / p.T);
+  const long long x0 = (long long)tau * p.T;
+  w.tile = p.dp_tiles + tau;
+  w.kb = int(x - x0);
+  w.ke = int(e - x0 < p.T ? e - x0 : p.T);
+  w.sk = (w.kb == 0 && w.ke == p.T) ? -1 : tau;
+  return true;
+}
+
+// Stores one lane-quarter's 32 rows x 256 columns of C from accumulator
+// columns `acc` (rows m0 + lane, columns n0 ..).
+__device__ __forceinline__ void store_c_quarter(uint32_t acc, float* crow,
+                                                bool row_ok, int n0,
+                                                const PairParams& p) {
+#pragma unroll 1
+  for (int cb = 0; cb < PN / 32; ++cb) {
+    uint32_t v[32];
+    tc::tmem_ld_32x32b_x32(acc + 32 * cb, v);
+    tc::tmem_ld_wait();
+    if (!row_ok) continue;
+    const int c0 = n0 + 32 * cb;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const int c = c0 + e;
+      if (p.vec_store && c + 3 < p.N) {
+        *reinterpret_cast<float4*>(crow + c) =
+            make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c + u < p.N) crow[c + u] = __uint_as_float(v[e + u]);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(P_THREADS, 1)
 k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
-              const __grid_constant__ CUtensorMap tmB, float* __restrict__ C,
-              int M, int N, int K, long long ldc, int tiles_m, int tiles_n,
-              int vec_store, int* status) {
+              const __grid_constant__ CUtensorMap tmB, const PairParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -319,8 +426,10 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
   const uint32_t conv0 = full0 + 8 * XSTAGES;     // own split done
   const uint32_t empty0 = conv0 + 8 * XSTAGES;    // pair MMAs done reading
   const uint32_t peer0 = empty0 + 8 * XSTAGES;    // odd block split (even)
-  const uint32_t accf = peer0 + 8 * XSTAGES;      // accumulator complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (4 * XSTAGES + 1));
+  const uint32_t accf0 = peer0 + 8 * XSTAGES;     // accumulator b complete
+  const uint32_t acce0 = accf0 + 16;              // accumulator b read (even)
+  const uint32_t drain = acce0 + 16;              // teardown (even)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (4 * XSTAGES + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto A_of = [&](int s) { return smem + s * X_STAGE; };
   auto Alo_of = [&](int s) { return smem + s * X_STAGE + X_A_BYTES; };
@@ -331,12 +440,7 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
-  int pm, pn;
-  tile_of(blockIdx.x >> 1, tiles_m, tiles_n, pm, pn);
-  const int m_own = pm * PM + 128 * int(rank);  // this block's rows
-  const int n_pair = pn * PN;                   // the pair's columns
-  const int n_own = n_pair + 128 * int(rank);   // this block's B columns
-  const int T = (K + XK - 1) / XK;
+  const int cl = int(blockIdx.x >> 1);
 
   if (tid == 0) {
     for (int s = 0; s < XSTAGES; ++s) {
@@ -345,7 +449,11 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       mbar_init(empty0 + 8 * s, 1);
       mbar_init(peer0 + 8 * s, 1);
     }
-    mbar_init(accf, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, P_EPI_ARRIVALS);
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
@@ -364,122 +472,238 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
   if (warp == 0) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      for (int t = 0; t < T && !*abort_flag; ++t) {
-        const int s = t % XSTAGES;
-        if (t >= XSTAGES &&
-            !mbar_wait_bounded(empty0 + 8 * s, ((t / XSTAGES) - 1) & 1, status,
-                               kSiteTf32Empty, kWaitLimitNs)) {
-          *abort_flag = 1;
-          break;
+      int g = 0;  // stages issued
+      Unit w;
+      for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
+        int pm, pn;
+        tile_of(w.tile, p.tiles_m, p.tiles_n, pm, pn);
+        const int m_own = pm * PM + 128 * int(rank);
+        const int n_own = pn * PN + 128 * int(rank);
+        for (int k = w.kb; k < w.ke; ++k, ++g) {
+          const int s = g % XSTAGES;
+          if (g >= XSTAGES &&
+              !mbar_wait_bounded(empty0 + 8 * s, ((g / XSTAGES) - 1) & 1,
+                                 p.status, kSiteTf32Empty, kWaitLimitNs)) {
+            *abort_flag = 1;
+            break;
+          }
+          const uint32_t bar = full0 + 8 * s;
+          mbar_arrive_expect_tx(bar, X_A_BYTES + X_B_BYTES);
+          tma_load_2d(smem_u32(A_of(s)), &tmA, k * XK, m_own, bar);
+          for (int j = 0; j < 128 / 32; ++j)
+            tma_load_2d(smem_u32(B_of(s) + j * X_B_BOX), &tmB, n_own + 32 * j,
+                        k * XK, bar);
         }
-        const uint32_t bar = full0 + 8 * s;
-        mbar_arrive_expect_tx(bar, X_A_BYTES + X_B_BYTES);
-        tma_load_2d(smem_u32(A_of(s)), &tmA, t * XK, m_own, bar);
-        for (int j = 0; j < 128 / 32; ++j)
-          tma_load_2d(smem_u32(B_of(s) + j * X_B_BOX), &tmB, n_own + 32 * j,
-                      t * XK, bar);
       }
+      // Let the last loads land before the block can exit (they complete
+      // even when nobody consumes them).
+      for (int d = g - XSTAGES < 0 ? 0 : g - XSTAGES; d < g; ++d)
+        mbar_wait_bounded(full0 + 8 * (d % XSTAGES), (d / XSTAGES) & 1,
+                          p.status, kSiteTf32Full, kWaitLimitNs / 100);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issue
     if (lane == 0 && rank == 0) {
+      // -------------------------------------------------------- MMA issue
       constexpr uint32_t idesc = tc::idesc_tf32(PM, PN, false, false);
-      for (int t = 0; t < T; ++t) {
-        const int s = t % XSTAGES;
-        const uint32_t par = (t / XSTAGES) & 1;
-        if (*abort_flag ||
-            !mbar_wait_bounded(conv0 + 8 * s, par, status, kSiteTf32Conv,
-                               kWaitLimitNs) ||
-            !mbar_wait_bounded<true>(peer0 + 8 * s, par, status,
-                                     kSiteTf32Peer, kWaitLimitNs)) {
+      int g = 0;
+      Unit w;
+      for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
+        const int b = u & 1;
+        if (u >= 2 &&
+            !mbar_wait_bounded<true>(acce0 + 8 * b, ((u >> 1) - 1) & 1,
+                                     p.status, kSiteTf32Acc, kWaitLimitNs)) {
           *abort_flag = 1;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t a = smem_u32(A_of(s)), al = smem_u32(Alo_of(s));
-        const uint32_t b = smem_u32(B_of(s)), bl = smem_u32(Blo_of(s));
+        const uint32_t acc = tmem + uint32_t(b * P_ACC_COLS);
+        for (int k = w.kb; k < w.ke; ++k, ++g) {
+          const int s = g % XSTAGES;
+          const uint32_t par = (g / XSTAGES) & 1;
+          if (*abort_flag ||
+              !mbar_wait_bounded(conv0 + 8 * s, par, p.status, kSiteTf32Conv,
+                                 kWaitLimitNs) ||
+              !mbar_wait_bounded<true>(peer0 + 8 * s, par, p.status,
+                                       kSiteTf32Peer, kWaitLimitNs)) {
+            *abort_flag = 1;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t a = smem_u32(A_of(s)), al = smem_u32(Alo_of(s));
+          const uint32_t bb = smem_u32(B_of(s)), bl = smem_u32(Blo_of(s));
 #pragma unroll
-        for (int ks = 0; ks < XK / 8; ++ks) {
-          const uint64_t da = tc::smem_desc(a + 32 * ks, 16, 1024,
-                                            tc::kLayoutSwizzle128);
-          const uint64_t dal = tc::smem_desc(al + 32 * ks, 16, 1024,
-                                             tc::kLayoutSwizzle128);
-          const uint64_t db = tc::smem_desc(b + 32 * ks, 16, 1024,
-                                            tc::kLayoutSwizzle128);
-          const uint64_t dbl = tc::smem_desc(bl + 32 * ks, 16, 1024,
-                                             tc::kLayoutSwizzle128);
-          tc::mma_tf32_pair(tmem, dal, db, idesc, (t > 0 || ks > 0) ? 1u : 0u);
-          tc::mma_tf32_pair(tmem, da, dbl, idesc, 1u);
-          tc::mma_tf32_pair(tmem, da, db, idesc, 1u);
+          for (int ks = 0; ks < XK / 8; ++ks) {
+            const uint64_t da = tc::smem_desc(a + 32 * ks, 16, 1024,
+                                              tc::kLayoutSwizzle128);
+            const uint64_t dal = tc::smem_desc(al + 32 * ks, 16, 1024,
+                                               tc::kLayoutSwizzle128);
+            const uint64_t db = tc::smem_desc(bb + 32 * ks, 16, 1024,
+                                              tc::kLayoutSwizzle128);
+            const uint64_t dbl = tc::smem_desc(bl + 32 * ks, 16, 1024,
+                                               tc::kLayoutSwizzle128);
+            tc::mma_tf32_pair(acc, dal, db, idesc,
+                              (k > w.kb || ks > 0) ? 1u : 0u);
+            tc::mma_tf32_pair(acc, da, dbl, idesc, 1u);
+            tc::mma_tf32_pair(acc, da, db, idesc, 1u);
+          }
+          tc::commit_pair_multicast(empty0 + 8 * s, 0x3);
         }
-        tc::commit_pair_multicast(empty0 + 8 * s, 0x3);
+        if (*abort_flag) break;
+        tc::commit_pair_multicast(accf0 + 8 * b, 0x3);
       }
-      tc::commit_pair_multicast(accf, 0x3);
+      // Every MMA issued has finished before the blocks may exit.
+      tc::commit_pair_multicast(drain, 0x1);
+      mbar_wait_bounded(drain, 0, p.status, kSiteTf32Acc, kWaitLimitNs);
     } else if (lane == 0) {
-      // odd block: forward each completed split to the even block. The
-      // acquire of the local wait and the cumulative cluster-scope release
-      // order all four split warps' writes before the even block's MMAs.
+      // ----------------------------------------- odd block: forward splits
+      // The acquire of the local wait and the cumulative cluster-scope
+      // release order all four split warps' writes before the even block's
+      // MMAs.
       const uint32_t peer_leader = cluster_map(peer0, 0);
-      for (int t = 0; t < T; ++t) {
-        const int s = t % XSTAGES;
+      int g = 0;
+      Unit w;
+      for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
+        for (int k = w.kb; k < w.ke; ++k, ++g) {
+          const int s = g % XSTAGES;
+          if (*abort_flag ||
+              !mbar_wait_bounded(conv0 + 8 * s, (g / XSTAGES) & 1, p.status,
+                                 kSiteTf32Conv, kWaitLimitNs)) {
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_cluster(peer_leader + 8 * s);
+        }
+      }
+    }
+  } else if (warp < P_EPI_WARP0) {
+    // ---------------------------------------------------------- split
+    const int ct = tid - 64;  // 0..127
+    int g = 0;
+    Unit w;
+    for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
+      for (int k = w.kb; k < w.ke; ++k, ++g) {
+        const int s = g % XSTAGES;
         if (*abort_flag ||
-            !mbar_wait_bounded(conv0 + 8 * s, (t / XSTAGES) & 1, status,
-                               kSiteTf32Conv, kWaitLimitNs)) {
+            !mbar_wait_bounded(full0 + 8 * s, (g / XSTAGES) & 1, p.status,
+                               kSiteTf32Full, kWaitLimitNs)) {
           *abort_flag = 1;
           break;
         }
-        mbar_arrive_cluster(peer_leader + 8 * s);
+#pragma unroll
+        for (int q = 0; q < X_A_BYTES / 16 / X_CONV_THREADS; ++q)
+          split4(A_of(s), Alo_of(s), ct + X_CONV_THREADS * q);
+        split_transpose_box(B_of(s) + (warp - 2) * X_B_BOX,
+                            Blo_of(s) + (warp - 2) * X_B_BOX, lane);
+        fence_async_shared();  // generic writes -> visible to the MMA
+        __syncwarp();
+        if (lane == 0) mbar_arrive(conv0 + 8 * s);
       }
     }
   } else {
-    // ---------------------------------------------------------- split
-    const int ct = tid - 64;  // 0..127
-    for (int t = 0; t < T; ++t) {
-      const int s = t % XSTAGES;
-      if (*abort_flag ||
-          !mbar_wait_bounded(full0 + 8 * s, (t / XSTAGES) & 1, status,
-                             kSiteTf32Full, kWaitLimitNs)) {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // tensor-memory lanes of this warp
+    const int row = 32 * quarter + lane;  // row within the block's half
+    const uint32_t acce_leader = cluster_map(acce0, 0);
+    float4* ws4 = reinterpret_cast<float4*>(p.ws);
+    Unit w;
+    for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
+      const int b = u & 1;
+      if (!mbar_wait_bounded(accf0 + 8 * b, (u >> 1) & 1, p.status,
+                             kSiteTf32Acc, kWaitLimitNs)) {
         *abort_flag = 1;
         break;
       }
-#pragma unroll
-      for (int q = 0; q < X_A_BYTES / 16 / X_CONV_THREADS; ++q)
-        split4(A_of(s), Alo_of(s), ct + X_CONV_THREADS * q);
-      split_transpose_box(B_of(s) + (warp - 2) * X_B_BOX,
-                          Blo_of(s) + (warp - 2) * X_B_BOX, lane);
-      fence_async_shared();  // generic writes -> visible to the MMA
-      __syncwarp();
-      if (lane == 0) mbar_arrive(conv0 + 8 * s);
-    }
-    // ---------------------------------------------------------- epilogue
-    const bool ok = mbar_wait_bounded(accf, 0, status, kSiteTf32Acc,
-                                      *abort_flag ? kWaitLimitNs / 100
-                                                  : kWaitLimitNs);
-    tc::fence_after_sync();
-    const int quarter = warp & 3;
-    const int r = m_own + 32 * quarter + lane;
-    float* crow = C + (long long)r * ldc;
+      tc::fence_after_sync();
+      const uint32_t acc = tmem + uint32_t(b * P_ACC_COLS) +
+                           (uint32_t(32 * quarter) << 16);
+      int pm, pn;
+      tile_of(w.tile, p.tiles_m, p.tiles_n, pm, pn);
+      const int r = pm * PM + 128 * int(rank) + row;
+      const int n0 = pn * PN;
+      float* crow = p.C + (long long)r * p.ldc;
+      int slot = 0;
+      if (w.sk < 0) {
+        store_c_quarter(acc, crow, r < p.M, n0, p);
+      } else {
+        // this block's piece: thread-major float4s, coalesced per warp
+        const long long x0 = (long long)w.sk * p.T;
+        slot = sk_begin(cl, p) >= x0 ? 0 : 1;
+        float4* piece = ws4 + ((long long)(cl * 2 + slot) * 2 + rank) *
+                                  (P_PIECE_FLOATS / 4);
 #pragma unroll 1
-    for (int cb = 0; cb < PN / 32; ++cb) {
-      uint32_t v[32];
-      tc::tmem_ld_32x32b_x32(tmem + (uint32_t(32 * quarter) << 16) + 32 * cb,
-                             v);
-      tc::tmem_ld_wait();
-      if (!ok || *abort_flag || r >= M) continue;
-      const int c0 = n_pair + 32 * cb;
+        for (int cb = 0; cb < PN / 32; ++cb) {
+          uint32_t v[32];
+          tc::tmem_ld_32x32b_x32(acc + 32 * cb, v);
+          tc::tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const int c = c0 + e;
-        if (vec_store && c + 3 < N) {
-          *reinterpret_cast<float4*>(crow + c) =
-              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                          __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-        } else {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (c + u < N) crow[c + u] = __uint_as_float(v[e + u]);
+          for (int e = 0; e < 8; ++e)
+            __stcg(piece + (cb * 8 + e) * 128 + row,
+                   make_float4(__uint_as_float(v[4 * e]),
+                               __uint_as_float(v[4 * e + 1]),
+                               __uint_as_float(v[4 * e + 2]),
+                               __uint_as_float(v[4 * e + 3])));
         }
       }
+      // accumulator b may be overwritten by the next unit's MMAs
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(acce0 + 8 * b);
+        else
+          mbar_arrive_cluster(acce_leader + 8 * b);
+      }
+      if (w.sk < 0) continue;
+      // ------------------------------------------------ stream-K fixup
+      __threadfence();
+      __syncwarp();
+      int* counter = p.counters + (w.sk * 2 + int(rank)) * 4 + quarter;
+      int arrived = 0;
+      if (lane == 0) arrived = atomicAdd(counter, 1);
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      const long long x0 = (long long)w.sk * p.T;
+      const int c_first = sk_owner(x0, p);
+      const int pieces = sk_owner(x0 + p.T - 1, p) - c_first + 1;
+      if (arrived != pieces - 1) continue;
+      __threadfence();
+      const bool row_ok = r < p.M;
+#pragma unroll 1
+      for (int cb = 0; cb < PN / 32; ++cb) {
+        float4 sum[8];
+        for (int j = 0; j < pieces; ++j) {
+          const int cj = c_first + j;
+          const int sj = sk_begin(cj, p) >= x0 ? 0 : 1;
+          const float4* pj = ws4 + ((long long)(cj * 2 + sj) * 2 + rank) *
+                                       (P_PIECE_FLOATS / 4);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 x = __ldcg(pj + (cb * 8 + e) * 128 + row);
+            if (j == 0) {
+              sum[e] = x;
+            } else {
+              sum[e].x += x.x;
+              sum[e].y += x.y;
+              sum[e].z += x.z;
+              sum[e].w += x.w;
+            }
+          }
+        }
+        if (!row_ok) continue;
+        const int c0 = n0 + 32 * cb;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = c0 + 4 * e;
+          if (p.vec_store && c + 3 < p.N) {
+            *reinterpret_cast<float4*>(crow + c) = sum[e];
+          } else {
+            const float s4[4] = {sum[e].x, sum[e].y, sum[e].z, sum[e].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (c + q < p.N) crow[c + q] = s4[q];
+          }
+        }
+      }
+      if (lane == 0) *counter = 0;
     }
   }
   tc::fence_before_sync();
@@ -493,26 +717,101 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
 
 }  // namespace
 
-cudaError_t tf32x3_init() {
-  const cudaError_t e = cudaFuncSetAttribute(
+cudaError_t tf32x3_init(int* pair_clusters) {
+  cudaError_t e = cudaFuncSetAttribute(
       k_tf32x3, cudaFuncAttributeMaxDynamicSharedMemorySize, int(X_SMEM));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_tf32x3_pair,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(X_SMEM));
+  e = cudaFuncSetAttribute(k_tf32x3_pair,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(P_SMEM));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(P_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = P_SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, k_tf32x3_pair, &cfg);
+  if (e != cudaSuccess) return e;
+  *pair_clusters = n;
+  return n > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+PairPlan plan_pair(int64_t M, int64_t N, int64_t K, int clusters,
+                   bool stream_k) {
+  PairPlan pl;
+  pl.tiles_m = int((M + PM - 1) / PM);
+  pl.tiles_n = int((N + PN - 1) / PN);
+  pl.tiles = pl.tiles_m * pl.tiles_n;
+  pl.T = int((K + XK - 1) / XK);
+  if (clusters < 1) clusters = 1;
+  pl.G = pl.tiles < clusters ? pl.tiles : clusters;
+  pl.dp_tiles = pl.tiles;
+  pl.sk_tiles = 0;
+  const int64_t rem = pl.tiles % clusters;
+  if (stream_k && rem != 0) {
+    if (pl.tiles < clusters) {
+      // One partial wave: spread all k-slices over more clusters, when whole
+      // tiles would leave over a quarter of them idle (above that, the
+      // fix-up costs more than the idle clusters).
+      const int64_t by_work = 4 * pl.tiles <= 3 * int64_t(clusters)
+                                  ? int64_t(pl.tiles) * pl.T / kPairMinSkIters
+                                  : 0;
+      const int64_t G = by_work < clusters ? by_work : clusters;
+      if (G > pl.tiles) {
+        pl.G = int(G);
+        pl.sk_tiles = pl.tiles;
+        pl.dp_tiles = 0;
+      }
+    } else {
+      int64_t sk = rem;
+      if (sk * pl.T / clusters < kPairMinSkIters) sk += clusters;
+      if (sk * pl.T / clusters >= kPairMinSkIters) {  // else: short K
+        pl.G = clusters;
+        pl.sk_tiles = int(sk);
+        pl.dp_tiles = pl.tiles - pl.sk_tiles;
+      }
+    }
+  }
+  pl.sk_iters = int64_t(pl.sk_tiles) * pl.T;
+  pl.ws_floats =
+      pl.sk_tiles ? size_t(pl.G) * 2 * 2 * size_t(P_PIECE_FLOATS) : 0;
+  pl.counters = size_t(pl.sk_tiles) * 2 * 4;
+  return pl;
 }
 
 cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
-                               const CUtensorMap& tmB, int* status,
+                               const CUtensorMap& tmB, const PairPlan& pl,
+                               float* ws, int* counters, int* status,
                                cudaStream_t s) {
-  const int tiles_m = int((g.M + PM - 1) / PM);
-  const int tiles_n = int((g.N + PN - 1) / PN);
-  const bool vec = (g.ldc % 4 == 0) &&
-                   (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
+  PairParams p;
+  p.C = g.C;
+  p.M = int(g.M);
+  p.N = int(g.N);
+  p.K = int(g.K);
+  p.ldc = (long long)g.ldc;
+  p.tiles_m = pl.tiles_m;
+  p.tiles_n = pl.tiles_n;
+  p.T = pl.T;
+  p.G = pl.G;
+  p.dp_tiles = pl.dp_tiles;
+  p.sk_tiles = pl.sk_tiles;
+  p.sk_iters = (long long)pl.sk_iters;
+  p.ws = ws;
+  p.counters = counters;
+  p.vec_store = (g.ldc % 4 == 0) &&
+                (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
+  p.status = status;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2u * unsigned(tiles_m) * unsigned(tiles_n), 1, 1);
-  cfg.blockDim = dim3(X_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = X_SMEM;
+  cfg.gridDim = dim3(2u * unsigned(pl.G), 1, 1);
+  cfg.blockDim = dim3(P_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = P_SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -521,9 +820,7 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_tf32x3_pair, tmA, tmB, g.C, int(g.M),
-                            int(g.N), int(g.K), (long long)g.ldc, tiles_m,
-                            tiles_n, vec ? 1 : 0, status);
+  return cudaLaunchKernelEx(&cfg, k_tf32x3_pair, tmA, tmB, p);
 }
 
 cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,

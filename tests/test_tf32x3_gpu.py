@@ -120,3 +120,63 @@ def test_deterministic(path):
     C2 = dfm.matmul(A, B, path=path)
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
+
+
+# Shapes that drive each branch of the pair kernel's persistent schedule on
+# a 152-SM part (76 clusters): whole waves plus a stream-K tail, a tail
+# widened by one wave (one tile over a wave), every tile split by k-slices
+# (fewer tiles than clusters), whole tiles only (short K), and ragged edges
+# in M, N and K inside split tiles.
+PAIR_SCHEDULES = [
+    (4096, 4096, 4096),    # 228 whole + 28 split
+    (1792, 2816, 1024),    # 77 tiles: the split part widened to 77
+    (1000, 1000, 1000),    # 16 tiles over 64 clusters
+    (2048, 2048, 2048),    # 64 tiles over 76 clusters
+    (4096, 4096, 64),      # 2 k-slices: whole tiles, round robin
+    (2300, 2900, 1900),    # ragged M, N, K; split tiles at the edges
+    (20000, 260, 516),     # tall and thin
+]
+
+
+@pytest.mark.parametrize("mnk", PAIR_SCHEDULES, ids=str)
+@pytest.mark.parametrize("kind", ["uniform", "integers"])
+def test_pair_schedules(mnk, kind):
+    run_case(*mnk, kind=kind, seed=sum(mnk) % 1000, path=PAIR)
+
+
+def test_pair_split_tiles_deterministic():
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    A = torch.from_numpy(matgen.normal(5, 0, 2300, 1900)).cuda()
+    B = torch.from_numpy(matgen.normal(5, 1, 1900, 2900)).cuda()
+    outs = [dfm.matmul(A, B, path=PAIR) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+def test_concurrent_streams_do_not_share_partials():
+    # Two unordered streams run split-tile products at the same time; each
+    # stream has its own stream-K workspace, so both match the serial result.
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    A = torch.from_numpy(matgen.uniform(6, 0, 2300, 1900)).cuda()
+    B = torch.from_numpy(matgen.uniform(6, 1, 1900, 2900)).cuda()
+    A2 = torch.from_numpy(matgen.uniform(7, 0, 2300, 1900)).cuda()
+    ref = dfm.matmul(A, B, path=PAIR)
+    ref2 = dfm.matmul(A2, B, path=PAIR)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(4):
+        C1 = torch.empty_like(ref)
+        C2 = torch.empty_like(ref)
+        with torch.cuda.stream(s1):
+            dfm.matmul(A, B, out=C1, path=PAIR)
+        with torch.cuda.stream(s2):
+            dfm.matmul(A2, B, out=C2, path=PAIR)
+        outs.append((C1, C2))
+    torch.cuda.synchronize()
+    assert dfm.sgemm_watchdog_status() == (0, 0)
+    for C1, C2 in outs:
+        assert torch.equal(C1, ref)
+        assert torch.equal(C2, ref2)
