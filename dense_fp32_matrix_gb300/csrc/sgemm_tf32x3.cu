@@ -84,6 +84,20 @@ __device__ __forceinline__ void split4(uint8_t* hi_buf, uint8_t* lo_buf,
   *lp = l;
 }
 
+// As split4, but leaves x in place as the high part: the MMA reads an fp32
+// operand as TF32 by ignoring its 13 low mantissa bits, which is the same
+// hi as above (Inf and NaN included), so only lo is written.
+__device__ __forceinline__ void split4_lo(const uint8_t* x_buf, uint8_t* lo_buf,
+                                          int idx) {
+  const float4 x = reinterpret_cast<const float4*>(x_buf)[idx];
+  float4 h, l;
+  split_tf32(x.x, h.x, l.x);
+  split_tf32(x.y, h.y, l.y);
+  split_tf32(x.z, h.z, l.z);
+  split_tf32(x.w, h.w, l.w);
+  reinterpret_cast<float4*>(lo_buf)[idx] = l;
+}
+
 // Box j of a B stage (32 k rows x 32 n, N-major, TMA 128-byte swizzle) ->
 // K-major rows n = 32 j + lane of B (hi, in place) and B_lo.
 __device__ __forceinline__ void split_transpose_box(uint8_t* box, uint8_t* lo_box,
@@ -103,6 +117,55 @@ __device__ __forceinline__ void split_transpose_box(uint8_t* box, uint8_t* lo_bo
     split_tf32(x[4 * c + 2], h.z, l.z);
     split_tf32(x[4 * c + 3], h.w, l.w);
     const int off = lane * 128 + ((c ^ (lane & 7)) << 4);
+    *reinterpret_cast<float4*>(box + off) = h;
+    *reinterpret_cast<float4*>(lo_box + off) = l;
+  }
+}
+
+// Named barrier over `threads` threads (a multiple of 32) with id 1..15.
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// All of `threads` threads at named barrier `id` learn whether every one of
+// them passed pred != 0.
+__device__ __forceinline__ bool named_all(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// Half of split_transpose_box for two warps sharing a box: this warp reads
+// k rows 16 half .. 16 half + 15 (column n = 32 j + lane), waits until the
+// other warp has read its half too (the box is rewritten in place), then
+// writes the matching 16-k half of K-major row n (hi in place, and B_lo).
+__device__ __forceinline__ void split_transpose_half(uint8_t* box,
+                                                    uint8_t* lo_box, int lane,
+                                                    int half, int bar_id) {
+  float x[16];
+  const int cb = (lane * 4) / 16, cw = (lane * 4) % 16;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int kk = 16 * half + k;
+    x[k] = *reinterpret_cast<const float*>(box + kk * 128 +
+                                           ((cb ^ (kk & 7)) << 4) + cw);
+  }
+  named_sync(bar_id, 64);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float4 h, l;
+    split_tf32(x[4 * c + 0], h.x, l.x);
+    split_tf32(x[4 * c + 1], h.y, l.y);
+    split_tf32(x[4 * c + 2], h.z, l.z);
+    split_tf32(x[4 * c + 3], h.w, l.w);
+    const int off = lane * 128 + (((4 * half + c) ^ (lane & 7)) << 4);
     *reinterpret_cast<float4*>(box + off) = h;
     *reinterpret_cast<float4*>(lo_box + off) = l;
   }
@@ -301,24 +364,28 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
 // and the last of the tile's pieces to arrive adds them all in k order and
 // stores C (no cluster waits on another; the sum order is fixed).
 //
-// Roles in each block (320 threads):
+// Roles in each block (448 threads):
 //   warp 0      TMA producer over the cluster's units, one ring of stages;
 //   warp 1      even block: allocates 512 tensor-memory columns (two
 //               256-column accumulators) for both blocks and issues the
 //               MMAs; odd block: forwards each completed split to the even
 //               block with one cluster-scope release (one fence per stage
 //               rather than one per split warp);
-//   warps 2..5  split and transpose each landed stage (as above) and arrive
-//               on their own block's split barrier;
-//   warps 6..9  epilogue, one tensor-memory lane quarter each: read a
+//   warps 2..9  split and transpose each landed stage and arrive on their
+//               own block's split barrier; two warps share each B box, one
+//               per 16-k half (eight warps halve the split's latency, which
+//               sits on the path from a freed stage to its next MMAs);
+//   warps 10..13 epilogue, one tensor-memory lane quarter each: read a
 //               finished accumulator, store C or the piece, hand the
 //               accumulator back. With two accumulators the MMAs of the
 //               next unit run while the previous one is stored.
 constexpr int PM = 256, PN = 256;
-constexpr int P_THREADS = 320;
+constexpr int P_THREADS = 448;
+constexpr int P_CONV_WARPS = 8;
+constexpr int P_CONV_THREADS = 32 * P_CONV_WARPS;
 constexpr int P_ACC_COLS = 256;                      // one accumulator
 constexpr int P_TMEM_COLS = 2 * P_ACC_COLS;
-constexpr int P_EPI_WARP0 = 6;
+constexpr int P_EPI_WARP0 = 2 + P_CONV_WARPS;
 constexpr int P_EPI_ARRIVALS = 2 * 4;                // 4 warps x 2 blocks
 constexpr int P_PIECE_FLOATS = 128 * PN;             // one block's half tile
 constexpr size_t P_SMEM = size_t(XSTAGES) * X_STAGE + 1024 + 256;
@@ -445,7 +512,7 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
   if (tid == 0) {
     for (int s = 0; s < XSTAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(conv0 + 8 * s, X_CONV_THREADS / 32);
+      mbar_init(conv0 + 8 * s, P_CONV_WARPS);
       mbar_init(empty0 + 8 * s, 1);
       mbar_init(peer0 + 8 * s, 1);
     }
@@ -577,23 +644,30 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
     }
   } else if (warp < P_EPI_WARP0) {
     // ---------------------------------------------------------- split
-    const int ct = tid - 64;  // 0..127
+    const int ct = tid - 64;  // 0..255
+    const int box = (warp - 2) >> 1, half = (warp - 2) & 1;
+    const int bar_id = 1 + box;  // named barrier of this box's two warps
     int g = 0;
+    bool ok = true;
     Unit w;
-    for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
+    // The two warps of a box take every continue/abort decision together
+    // (bar.red), so neither can leave the other waiting at a named barrier.
+    for (int u = 0; ok && unit_of(cl, u, p, w); ++u) {
       for (int k = w.kb; k < w.ke; ++k, ++g) {
         const int s = g % XSTAGES;
-        if (*abort_flag ||
-            !mbar_wait_bounded(full0 + 8 * s, (g / XSTAGES) & 1, p.status,
-                               kSiteTf32Full, kWaitLimitNs)) {
+        ok = !*abort_flag &&
+             mbar_wait_bounded(full0 + 8 * s, (g / XSTAGES) & 1, p.status,
+                               kSiteTf32Full, kWaitLimitNs);
+        ok = named_all(bar_id, 64, ok);
+        if (!ok) {
           *abort_flag = 1;
           break;
         }
 #pragma unroll
-        for (int q = 0; q < X_A_BYTES / 16 / X_CONV_THREADS; ++q)
-          split4(A_of(s), Alo_of(s), ct + X_CONV_THREADS * q);
-        split_transpose_box(B_of(s) + (warp - 2) * X_B_BOX,
-                            Blo_of(s) + (warp - 2) * X_B_BOX, lane);
+        for (int q = 0; q < X_A_BYTES / 16 / P_CONV_THREADS; ++q)
+          split4_lo(A_of(s), Alo_of(s), ct + P_CONV_THREADS * q);
+        split_transpose_half(B_of(s) + box * X_B_BOX,
+                             Blo_of(s) + box * X_B_BOX, lane, half, bar_id);
         fence_async_shared();  // generic writes -> visible to the MMA
         __syncwarp();
         if (lane == 0) mbar_arrive(conv0 + 8 * s);
