@@ -369,12 +369,11 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
 //   warp 1      even block: allocates 512 tensor-memory columns (two
 //               256-column accumulators) for both blocks and issues the
 //               MMAs; odd block: forwards each completed split to the even
-//               block with one cluster-scope release (one fence per stage
-//               rather than one per split warp);
+//               block with one arrival per stage;
 //   warps 2..9  split and transpose each landed stage and arrive on their
 //               own block's split barrier; two warps share each B box, one
-//               per 16-k half (eight warps halve the split's latency, which
-//               sits on the path from a freed stage to its next MMAs);
+//               per 16-k half (the split sits on the path from a freed
+//               stage to its next MMAs);
 //   warps 10..13 epilogue, one tensor-memory lane quarter each: read a
 //               finished accumulator, store C or the piece, hand the
 //               accumulator back. With two accumulators the MMAs of the
@@ -411,6 +410,22 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
       "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
           cluster_addr)
       : "memory");
+}
+
+// Arrive on a barrier of the other block with the default (CTA-scope)
+// release. Used for the split hand-over only: the split results and the
+// tensor core that reads them are on the same SM (this block's shared
+// memory), the writers made their stores visible to the async proxy
+// (fence.proxy.async) before arriving on this block's barrier, and the
+// CTA-scope release performs them in shared memory before the arrival
+// leaves the SM; the arrival only gates when the even block issues the MMA.
+// (The cluster-scope release costs about a thousand cycles per stage here,
+// on the refill path of every stage.) This is the cluster-barrier arrive of
+// the CUDA template library's 2-SM pipelines.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_addr)
+               : "memory");
 }
 
 __device__ __forceinline__ long long sk_begin(int c, const PairParams& p) {
@@ -623,9 +638,8 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       mbar_wait_bounded(drain, 0, p.status, kSiteTf32Acc, kWaitLimitNs);
     } else if (lane == 0) {
       // ----------------------------------------- odd block: forward splits
-      // The acquire of the local wait and the cumulative cluster-scope
-      // release order all four split warps' writes before the even block's
-      // MMAs.
+      // One arrival per stage once all split warps of this block are done
+      // (see mbar_arrive_remote for the ordering).
       const uint32_t peer_leader = cluster_map(peer0, 0);
       int g = 0;
       Unit w;
@@ -638,7 +652,7 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
             *abort_flag = 1;
             break;
           }
-          mbar_arrive_cluster(peer_leader + 8 * s);
+          mbar_arrive_remote(peer_leader + 8 * s);
         }
       }
     }
