@@ -40,6 +40,10 @@ CPU_SAMPLE_SECONDS = 12.0
 TF32_PER_BF16 = 1.1 / 2.25
 BF16_FALLBACK_TFLOPS = 1900.0   # used only when no measured peak is present
 TF32X3_PRODUCTS = 3             # TF32 tensor products per fp32 product
+# Dense TF32 tensor-core rate of one SM, ops per clock, as ncu reports it
+# for this part (the peak_sustained of the TF32 tensor-op counter; see
+# profiles/k_tf32x3_pair_square_4096.md).
+TF32_OPS_PER_CLK_PER_SM = 4096
 
 
 def flops(M, N, K):
@@ -389,6 +393,15 @@ def run_gpu(args, w):
                                                          eff_peak)),
                 "tensor_tflops": TF32X3_PRODUCTS * tflops,
                 "tensor_peak": tf32_peak}
+        # The same work against the hardware's dense TF32 rate at the SM
+        # clock seen while timing (what ncu's tensor-pipe counter measures):
+        # a fraction that cannot exceed 1.
+        hw_peak = sms * TF32_OPS_PER_CLK_PER_SM * peak_clock_mhz * 1e6 / 1e12
+        roof["tensor_pipe"] = {
+            "peak_tflops": hw_peak,
+            "frac": TF32X3_PRODUCTS * tflops / hw_peak,
+            "basis": ("%d SMs x %d dense TF32 ops/clk (ncu) x %.0f MHz"
+                      % (sms, TF32_OPS_PER_CLK_PER_SM, peak_clock_mhz))}
     else:
         roof = {"bound": "alu", "achieved": tflops, "peak": ffma_peak,
                 "unit": "TFLOP/s", "frac": tflops / ffma_peak,
