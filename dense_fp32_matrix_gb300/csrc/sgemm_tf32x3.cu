@@ -587,6 +587,13 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
     if (lane == 0 && rank == 0) {
       // -------------------------------------------------------- MMA issue
       constexpr uint32_t idesc = tc::idesc_tf32(PM, PN, false, false);
+      // completion of the pair's MMAs, signalled on the same barrier of
+      // both blocks (two commits; the odd block's barrier by its cluster
+      // address)
+      auto commit_both = [](uint32_t bar) {
+        tc::commit_pair(bar);
+        tc::commit_pair(cluster_map(bar, 1));
+      };
       int g = 0;
       Unit w;
       for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
@@ -628,13 +635,13 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
             tc::mma_tf32_pair(acc, da, dbl, idesc, 1u);
             tc::mma_tf32_pair(acc, da, db, idesc, 1u);
           }
-          tc::commit_pair_multicast(empty0 + 8 * s, 0x3);
+          commit_both(empty0 + 8 * s);  // stage s may be refilled
         }
         if (*abort_flag) break;
-        tc::commit_pair_multicast(accf0 + 8 * b, 0x3);
+        commit_both(accf0 + 8 * b);   // accumulator b complete
       }
       // Every MMA issued has finished before the blocks may exit.
-      tc::commit_pair_multicast(drain, 0x1);
+      tc::commit_pair(drain);
       mbar_wait_bounded(drain, 0, p.status, kSiteTf32Acc, kWaitLimitNs);
     } else if (lane == 0) {
       // ----------------------------------------- odd block: forward splits

@@ -130,14 +130,13 @@ __device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
-// Arrive once, in every CTA of `cta_mask`, on the mbarrier at this shared
-// offset when the pair's tcgen05 operations issued so far have completed.
-__device__ __forceinline__ void commit_pair_multicast(uint32_t mbar,
-                                                      uint16_t cta_mask) {
+// Pair form of commit: arrive once on the mbarrier at this shared::cluster
+// address (this CTA's or the peer's) when the pair's tcgen05 operations
+// issued so far by this thread have completed.
+__device__ __forceinline__ void commit_pair(uint32_t cluster_mbar) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
-      "multicast::cluster.b64 [%0], %1;" ::"r"(mbar),
-      "h"(cta_mask)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(cluster_mbar)
       : "memory");
 }
 
