@@ -180,3 +180,27 @@ def test_concurrent_streams_do_not_share_partials():
     for C1, C2 in outs:
         assert torch.equal(C1, ref)
         assert torch.equal(C2, ref2)
+
+
+# The pair kernel leaves the landed A in place as its TF32 high part (the
+# MMA reads an fp32 operand as TF32 by ignoring the 13 low mantissa bits);
+# the 1-SM kernel writes the masked high part. On schedules of whole tiles
+# both sum the same three products in the same k order, so the results must
+# agree bit for bit. Short K keeps the pair schedule to whole tiles on any
+# cluster count; 1024 x 4864 is one full wave of 76 pair tiles on a
+# 152-SM GB300.
+@pytest.mark.parametrize("mnk", [(4096, 4096, 64), (2048, 4096, 128),
+                                 (1024, 4864, 1000)], ids=str)
+@pytest.mark.parametrize("kind", ["uniform", "normal"])
+def test_pair_matches_masked_high_part_bitwise(mnk, kind):
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    M, N, K = mnk
+    if K > 128 and torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("one full wave of pair tiles needs 152 SMs")
+    A = torch.from_numpy(matgen.KINDS[kind](11, 0, M, K)).cuda()
+    B = torch.from_numpy(matgen.KINDS[kind](11, 1, K, N)).cuda()
+    C1 = dfm.matmul(A, B, path=PATH)
+    C2 = dfm.matmul(A, B, path=PAIR)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
