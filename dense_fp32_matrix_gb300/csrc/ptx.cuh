@@ -125,6 +125,17 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
                : "memory");
 }
 
+// Prefetch the 2-D box at {x, y} of the tensor map into L2 (no shared
+// memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map,
+                                                   int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y)
+      : "memory");
+}
+
 // 2-D tiled bulk tensor load global -> shared, completion signalled on the
 // mbarrier as transaction bytes. x is the innermost coordinate (elements),
 // y the outer one. Out-of-bounds box elements are filled with zero.

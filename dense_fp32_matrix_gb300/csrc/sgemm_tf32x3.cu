@@ -380,6 +380,7 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
 //               next unit run while the previous one is stored.
 constexpr int PM = 256, PN = 256;
 constexpr int P_THREADS = 448;
+constexpr int P_PREFETCH = 3;                        // k-slices ahead into L2
 constexpr int P_CONV_WARPS = 8;
 constexpr int P_CONV_THREADS = 32 * P_CONV_WARPS;
 constexpr int P_ACC_COLS = 256;                      // one accumulator
@@ -575,6 +576,13 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
           for (int j = 0; j < 128 / 32; ++j)
             tma_load_2d(smem_u32(B_of(s) + j * X_B_BOX), &tmB, n_own + 32 * j,
                         k * XK, bar);
+          // warm L2 with the tiles of a later k-slice of this unit, so that
+          // its load (issued when a stage frees up) is an L2 hit
+          if (k + P_PREFETCH < w.ke) {
+            tma_prefetch_l2_2d(&tmA, (k + P_PREFETCH) * XK, m_own);
+            for (int j = 0; j < 128 / 32; ++j)
+              tma_prefetch_l2_2d(&tmB, n_own + 32 * j, (k + P_PREFETCH) * XK);
+          }
         }
       }
       // Let the last loads land before the block can exit (they complete
