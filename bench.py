@@ -373,7 +373,13 @@ def run_gpu(args, w):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     dfm.sgemm_set_math_mode(prev_mode)
-    if e2e_plan == plan and not torch.equal(hC, C.cpu()):
+    # sgemm_host pipelines large products in row blocks, each computed as
+    # sgemm of that block, so it may differ from the one-piece product in
+    # the last bits: check it against the device result within twice the
+    # accuracy bound, with S_ij = sum_k |A_ik B_kj| bounded by
+    # (sum_k |A_ik|) * max |B| (no extra matrix product needed).
+    s_bound = A.abs().sum(dim=1, keepdim=True).cpu() * B.abs().max().item()
+    if not bool(((hC - C.cpu()).abs() <= 2e-4 * s_bound + 2e-6).all()):
         raise RuntimeError("e2e result differs from the device-path result")
 
     # The FP32 FMA roofline of this GPU at the clock seen while timing.

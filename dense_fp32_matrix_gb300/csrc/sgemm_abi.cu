@@ -477,6 +477,118 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
   }
 }
 
+// ---------------------------------------------------------------- host I/O
+//
+// sgemm_host for large products: the copies over the host link take longer
+// than the product itself, so they are overlapped with it. B goes first
+// (every row block of C needs all of it), then A in row blocks on a copy
+// stream; each row block of C is computed on the caller's stream as soon as
+// its rows of A have landed and is copied back on a second copy stream while
+// the next block computes. The copy streams are ordered after the caller's
+// earlier work by an event and the caller's stream waits for the last copy,
+// so the call stays asynchronous on `stream` with the same ordering as the
+// single-pass version.
+constexpr int kHostMaxChunks = 4;
+constexpr int64_t kHostChunkRows = 256;          // a pair tile's height
+
+struct HostPipe {
+  std::once_flag once;
+  int err = SGEMM_OK;
+  std::mutex mu;  // one call's enqueue sequence at a time (shared events)
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, b_ready = nullptr, done = nullptr;
+  cudaEvent_t a_ready[kHostMaxChunks] = {}, c_ready[kHostMaxChunks] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+
+// Row blocks for a product: one (no pipelining) below about 2^31
+// multiply-adds or 512 rows, else up to 4 blocks of whole 256-row tiles.
+int host_chunks(int64_t M, int64_t N, int64_t K) {
+  if (K == 0 || M < 2 * kHostChunkRows ||
+      double(M) * double(N) * double(K) < double(int64_t(1) << 31))
+    return 1;
+  const int64_t tiles = M / kHostChunkRows;
+  return int(tiles < kHostMaxChunks ? tiles : kHostMaxChunks);
+}
+
+int host_pipe(HostPipe** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+  HostPipe& hp = g_pipe[dev];
+  std::call_once(hp.once, [&] {
+    bool ok =
+        cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) ==
+            cudaSuccess &&
+        cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) ==
+            cudaSuccess &&
+        cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) ==
+            cudaSuccess &&
+        cudaEventCreateWithFlags(&hp.b_ready, cudaEventDisableTiming) ==
+            cudaSuccess &&
+        cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming) ==
+            cudaSuccess;
+    for (int i = 0; ok && i < kHostMaxChunks; ++i)
+      ok = cudaEventCreateWithFlags(&hp.a_ready[i], cudaEventDisableTiming) ==
+               cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.c_ready[i], cudaEventDisableTiming) ==
+               cudaSuccess;
+    hp.err = ok ? SGEMM_OK : SGEMM_ERR_CUDA;
+  });
+  *out = &hp;
+  return hp.err;
+}
+
+int host_pipelined(int64_t M, int64_t N, int64_t K, const float* hA,
+                   int64_t lda, const float* hB, int64_t ldb, float* hC,
+                   int64_t ldc, float* dA, float* dB, float* dC,
+                   cudaStream_t s, int chunks) {
+  HostPipe* hp = nullptr;
+  int rc = host_pipe(&hp);
+  if (rc != SGEMM_OK) return rc;
+  std::lock_guard<std::mutex> lock(hp->mu);
+  // row blocks on 256-row boundaries
+  int64_t r[kHostMaxChunks + 1];
+  const int64_t tiles = (M + kHostChunkRows - 1) / kHostChunkRows;
+  for (int i = 0; i <= chunks; ++i)
+    r[i] = i == chunks ? M : (tiles * i / chunks) * kHostChunkRows;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(cudaEventRecord(hp->start, s)) ||
+      !ok(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) ||
+      !ok(cudaStreamWaitEvent(hp->d2h, hp->start, 0)) ||
+      !ok(cudaMemcpy2DAsync(dB, size_t(N) * 4, hB, size_t(ldb) * 4,
+                            size_t(N) * 4, size_t(K), cudaMemcpyHostToDevice,
+                            hp->h2d)) ||
+      !ok(cudaEventRecord(hp->b_ready, hp->h2d)))
+    return SGEMM_ERR_CUDA;
+  for (int i = 0; i < chunks; ++i) {
+    const int64_t rows = r[i + 1] - r[i];
+    if (!ok(cudaMemcpy2DAsync(dA + r[i] * K, size_t(K) * 4, hA + r[i] * lda,
+                              size_t(lda) * 4, size_t(K) * 4, size_t(rows),
+                              cudaMemcpyHostToDevice, hp->h2d)) ||
+        !ok(cudaEventRecord(hp->a_ready[i], hp->h2d)))
+      return SGEMM_ERR_CUDA;
+  }
+  if (!ok(cudaStreamWaitEvent(s, hp->b_ready, 0))) return SGEMM_ERR_CUDA;
+  for (int i = 0; i < chunks; ++i) {
+    const int64_t rows = r[i + 1] - r[i];
+    if (!ok(cudaStreamWaitEvent(s, hp->a_ready[i], 0))) return SGEMM_ERR_CUDA;
+    rc = run(rows, N, K, dA + r[i] * K, K, dB, N, dC + r[i] * N, N, s,
+             SGEMM_PATH_AUTO);
+    if (rc != SGEMM_OK) return rc;
+    if (!ok(cudaEventRecord(hp->c_ready[i], s)) ||
+        !ok(cudaStreamWaitEvent(hp->d2h, hp->c_ready[i], 0)) ||
+        !ok(cudaMemcpy2DAsync(hC + r[i] * ldc, size_t(ldc) * 4, dC + r[i] * N,
+                              size_t(N) * 4, size_t(N) * 4, size_t(rows),
+                              cudaMemcpyDeviceToHost, hp->d2h)))
+      return SGEMM_ERR_CUDA;
+  }
+  if (!ok(cudaEventRecord(hp->done, hp->d2h)) ||
+      !ok(cudaStreamWaitEvent(s, hp->done, 0)))
+    return SGEMM_ERR_CUDA;
+  return SGEMM_OK;
+}
+
 }  // namespace dfm
 
 extern "C" {
@@ -521,6 +633,9 @@ int sgemm_host(int64_t M, int64_t N, int64_t K, const float* hA, int64_t lda,
   if (dC == nullptr || (K > 0 && (dA == nullptr || dB == nullptr)))
     return SGEMM_ERR_NULL_POINTER;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int chunks = dfm::host_chunks(M, N, K);
+  if (chunks > 1) return dfm::host_pipelined(M, N, K, hA, lda, hB, ldb, hC,
+                                             ldc, dA, dB, dC, s, chunks);
   if (K > 0) {
     if (cudaMemcpy2DAsync(dA, size_t(K) * 4, hA, size_t(lda) * 4,
                           size_t(K) * 4, size_t(M), cudaMemcpyHostToDevice,

@@ -136,10 +136,25 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
 /*
  * sgemm_host: C = A * B for HOST matrices hA (ld lda), hB (ld ldb), hC
  * (ld ldc). The caller provides device staging buffers dA (M*K floats),
- * dB (K*N floats) and dC (M*N floats), dense (ld = K, N, N). On `stream`:
- * copy hA -> dA and hB -> dB, run sgemm on the staging buffers, copy
- * dC -> hC. Asynchronous: hC is valid after the stream is synchronised; host
- * buffers should be pinned for the copies to overlap. Same errors as sgemm.
+ * dB (K*N floats) and dC (M*N floats), dense (ld = K, N, N). Copies hA ->
+ * dA and hB -> dB, runs the product on the staging buffers and copies
+ * dC -> hC, asynchronously with respect to the host and ordered on `stream`
+ * like any other work on it: it starts after the work enqueued on `stream`
+ * before the call, and work enqueued on `stream` after the call starts
+ * after hC has been written. hC is valid once the stream is synchronised.
+ * Host buffers should be pinned (pageable memory works, without overlap).
+ *
+ * Large products (M >= 512 rows and M*N*K >= 2^31) are pipelined: B is
+ * copied first, A in up to 4 row blocks of whole 256-row multiples on an
+ * internal copy stream; each row block of C is computed on `stream` as soon
+ * as its rows have landed and copied back on a second internal stream while
+ * the next block computes. Each row block is computed exactly as sgemm of
+ * that block, so the result meets the accuracy contract and is
+ * deterministic for a given shape, but may differ in the last bits from
+ * one sgemm of the whole product (the blocks can be scheduled differently).
+ * The internal streams and events are per device and shared by all calls;
+ * concurrent calls from several host threads are serialised while they
+ * enqueue. Same errors as sgemm.
  */
 int sgemm_host(int64_t M, int64_t N, int64_t K, const float* hA, int64_t lda,
                const float* hB, int64_t ldb, float* hC, int64_t ldc,
