@@ -18,8 +18,8 @@ import numpy as np
 
 from . import build as _build
 
-__all__ = ["gemm", "gemm_rows", "gemm_entries", "num_threads", "round_fp32",
-           "bound", "ORACLE_LIB"]
+__all__ = ["gemm", "gemm_ex", "gemm_rows", "gemm_entries", "num_threads",
+           "round_fp32", "bound", "ORACLE_LIB"]
 
 _lock = threading.Lock()
 _lib = None
@@ -49,6 +49,11 @@ def _load():
                                                 _fp, _i64, _ip, _ip, _i64,
                                                 _dp, _dp]
             lib.oracle_gemm_entries.restype = ctypes.c_int
+            lib.oracle_gemm_ex.argtypes = [ctypes.c_int, ctypes.c_int, _i64,
+                                           _i64, _i64, ctypes.c_double, _fp,
+                                           _i64, _fp, _i64, ctypes.c_double,
+                                           _fp, _i64, _dp, _i64, _dp, _i64]
+            lib.oracle_gemm_ex.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -97,6 +102,37 @@ def gemm(A, B, M=None, N=None, K=None, lda=None, ldb=None, order="outer",
     if rc != 0:
         raise ValueError("oracle rejected arguments (M=%d N=%d K=%d lda=%d "
                          "ldb=%d)" % (M, N, K, lda, ldb))
+    return C, S
+
+
+def gemm_ex(op_a, op_b, alpha, A, B, beta, C0, M, N, K, lda=None, ldb=None,
+            ldc0=None):
+    """``alpha * op(A) * op(B) + beta * C0`` in fp64; returns ``(C, S)``.
+
+    ``op_a`` / ``op_b`` are "N" or "T". A is stored M x K ("N", ld >= K) or
+    K x M ("T", ld >= M); B is stored K x N ("N", ld >= N) or N x K ("T",
+    ld >= K). C0 (M x N, ld ``ldc0``) is not read when beta == 0, A and B
+    are not read when alpha == 0 (pass None for unread operands).
+    """
+    oa, ob = {"N": 0, "T": 1}[op_a], {"N": 0, "T": 1}[op_b]
+    M, N, K = int(M), int(N), int(K)
+
+    def prep(X, cols):
+        if X is None:
+            return None, max(cols, 1)
+        X = np.ascontiguousarray(X, dtype=np.float32)
+        return X, (X.shape[1] if X.ndim == 2 else max(cols, 1))
+    A, lda_d = prep(A, M if oa else K)
+    B, ldb_d = prep(B, K if ob else N)
+    C0, ldc_d = prep(C0, N)
+    C = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_ex(oa, ob, M, N, K, float(alpha), _fptr(A),
+                                int(lda or lda_d), _fptr(B), int(ldb or ldb_d),
+                                float(beta), _fptr(C0), int(ldc0 or ldc_d),
+                                _dptr(C), max(N, 1), _dptr(S), max(N, 1))
+    if rc != 0:
+        raise ValueError("oracle rejected arguments")
     return C, S
 
 

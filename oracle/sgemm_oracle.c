@@ -172,3 +172,60 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K, const float *A,
   }
   return 0;
 }
+
+/*
+ * The general form C = alpha * op(A) * op(B) + beta * C0, in fp64:
+ *
+ *   op(A)_ik = A[i*lda + k]  (op_a == 0, A stored M x K)
+ *            = A[k*lda + i]  (op_a == 1, A stored K x M: op(A) = A^T)
+ *   op(B)_kj = B[k*ldb + j]  (op_b == 0, B stored K x N)
+ *            = B[j*ldb + k]  (op_b == 1, B stored N x K: op(B) = B^T)
+ *   C_ij = alpha * (sum_k op(A)_ik op(B)_kj) + beta * C0_ij
+ *   S_ij = |alpha| * (sum_k |op(A)_ik op(B)_kj|) + |beta * C0_ij|
+ *
+ * The pages print only alpha = 1, beta = 0 and row-major operands; the
+ * transposed forms and the scalars are the BLAS reading of the cuBLAS call
+ * they discuss ("GEMM from naive to tiled", sections 二.2 and 九.2): with
+ * beta == 0, C0 is not read (it may hold anything, NaN included); with
+ * alpha == 0 (or K == 0), A and B are not read. The K products are exact in
+ * fp64 and summed in ascending k as above; the sum is then scaled once.
+ */
+int oracle_gemm_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                   double alpha, const float *A, int64_t lda, const float *B,
+                   int64_t ldb, double beta, const float *C0, int64_t ldc0,
+                   double *C, int64_t ldc, double *S, int64_t lds) {
+  if ((op_a != 0 && op_a != 1) || (op_b != 0 && op_b != 1)) return -1;
+  if (M < 0 || N < 0 || K < 0) return -1;
+  const int64_t a_cols = op_a ? M : K, b_cols = op_b ? K : N;
+  if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1))
+    return -1;
+  const int read_ab = alpha != 0.0 && K > 0;
+  if (read_ab && M > 0 && N > 0 && (A == NULL || B == NULL)) return -1;
+  if (beta != 0.0 && M > 0 && N > 0 && (C0 == NULL || ldc0 < N)) return -1;
+  if (M > 0 && N > 0 && (C == NULL || ldc < N)) return -1;
+  if (S != NULL && M > 0 && N > 0 && lds < N) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      double acc = 0.0, mag = 0.0;
+      if (read_ab) {
+        for (int64_t k = 0; k < K; ++k) {
+          const double a = op_a ? (double)A[k * lda + i] : (double)A[i * lda + k];
+          const double b = op_b ? (double)B[j * ldb + k] : (double)B[k * ldb + j];
+          const double p = a * b;
+          acc += p;
+          mag += fabs(p);
+        }
+      }
+      double c = alpha * acc, s = fabs(alpha) * mag;
+      if (beta != 0.0) {
+        const double t = beta * (double)C0[i * ldc0 + j];
+        c += t;
+        s += fabs(t);
+      }
+      C[i * ldc + j] = c;
+      if (S != NULL) S[i * lds + j] = s;
+    }
+  }
+  return 0;
+}
