@@ -13,6 +13,7 @@ from . import _native
 
 __all__ = [
     "SgemmError", "sgemm", "sgemm_path", "sgemm_plan", "sgemm_host",
+    "sgemm_ex", "sgemm_plan_ex", "OPS",
     "sgemm_noalloc", "sgemm_set_math_mode", "MATH",
     "sgemm_watchdog_status", "sgemm_watchdog_selftest",
     "sgemm_status_string", "sgemm_path_name", "sgemm_version", "matmul",
@@ -77,6 +78,43 @@ def sgemm_path(M, N, K, A, lda, B, ldb, C, ldc, stream=None, path="auto"):
     _check(_native.lib().sgemm_path(M, N, K, _ptr(A), lda, _ptr(B), ldb,
                                     _ptr(C), ldc, _stream(stream),
                                     _path(path)), "sgemm_path")
+
+
+OPS = {"N": 0, "T": 1}
+
+
+def _op(op) -> int:
+    return OPS[op] if isinstance(op, str) else int(op)
+
+
+def sgemm_ex(op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+             stream=None, path="auto") -> None:
+    """C = alpha * op(A) * op(B) + beta * C on ``stream`` (async).
+
+    ``op_a`` / ``op_b`` are "N" (as stored) or "T" (stored transposed: A as
+    K x M, B as N x K). beta == 0 leaves C unread; alpha == 0 leaves A and B
+    unread. ``path`` forces a kernel path like ``sgemm_path``.
+    """
+    lib = _native.lib()
+    if path == "auto":
+        rc = lib.sgemm_ex(_op(op_a), _op(op_b), M, N, K, float(alpha),
+                          _ptr(A), lda, _ptr(B), ldb, float(beta), _ptr(C),
+                          ldc, _stream(stream))
+    else:
+        rc = lib.sgemm_ex_path(_op(op_a), _op(op_b), M, N, K, float(alpha),
+                               _ptr(A), lda, _ptr(B), ldb, float(beta),
+                               _ptr(C), ldc, _stream(stream), _path(path))
+    _check(rc, "sgemm_ex")
+
+
+def sgemm_plan_ex(op_a, op_b, M, N, K, lda, ldb, ldc, a_addr, b_addr,
+                  c_addr) -> str:
+    """Name of the kernel path ``sgemm_ex`` would take (host-only)."""
+    out = ctypes.c_int(-1)
+    _check(_native.lib().sgemm_plan_ex(_op(op_a), _op(op_b), M, N, K, lda,
+                                       ldb, ldc, a_addr, b_addr, c_addr,
+                                       ctypes.byref(out)), "sgemm_plan_ex")
+    return sgemm_path_name(out.value)
 
 
 def sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> None:

@@ -8,6 +8,36 @@
 
 namespace dfm {
 
+// The BLAS epilogue of every kernel: C = alpha * acc + beta * C_old, with
+// C_old not read when beta == 0 (alpha = 1, beta = 0 stores acc exactly).
+struct Scale {
+  float alpha = 1.f;
+  float beta = 0.f;
+};
+
+#ifdef __CUDACC__
+__device__ __forceinline__ float epi1(float acc, const float* c,
+                                      const Scale& sc) {
+  return sc.beta == 0.f ? sc.alpha * acc : fmaf(sc.alpha, acc, sc.beta * *c);
+}
+__device__ __forceinline__ float4 epi4(float4 v, const float* c,
+                                       const Scale& sc) {
+  if (sc.beta == 0.f)
+    return make_float4(sc.alpha * v.x, sc.alpha * v.y, sc.alpha * v.z,
+                       sc.alpha * v.w);
+  const float4 o = *reinterpret_cast<const float4*>(c);
+  return make_float4(fmaf(sc.alpha, v.x, sc.beta * o.x),
+                     fmaf(sc.alpha, v.y, sc.beta * o.y),
+                     fmaf(sc.alpha, v.z, sc.beta * o.z),
+                     fmaf(sc.alpha, v.w, sc.beta * o.w));
+}
+#endif
+
+// One product as the kernels see it: op(A) is M x K, op(B) is K x N.
+// op_a == 0: A stored M x K (lda >= K); 1: A stored K x M (lda >= M).
+// op_b == 0: B stored K x N (ldb >= N); 1: B stored N x K (ldb >= K).
+// Only the tensor-core kernels take op == 1; the dispatcher gives every
+// other kernel row-major copies.
 struct GemmArgs {
   int64_t M, N, K;
   const float* A;
@@ -16,6 +46,9 @@ struct GemmArgs {
   int64_t ldb;
   float* C;
   int64_t ldc;
+  Scale sc = Scale();
+  int op_a = 0;
+  int op_b = 0;
 };
 
 // Tile geometry of the main kernel (also used by the host dispatcher).
@@ -119,6 +152,12 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
 cudaError_t launch_gemv_row(const GemmArgs& g, int num_sms, cudaStream_t s);
 cudaError_t launch_gemv_col(const GemmArgs& g, int num_sms, cudaStream_t s);
 cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s);
+// out (cols x rows, dense, ld = rows) = in (rows x cols, ld) transposed.
+cudaError_t launch_transpose(const float* in, int64_t ld, int64_t rows,
+                             int64_t cols, float* out, cudaStream_t s);
+// C = beta * C over M x N (beta == 0: zeros, C not read).
+cudaError_t launch_scale_c(float* C, int64_t ldc, int64_t M, int64_t N,
+                           float beta, cudaStream_t s);
 
 // One block waiting on an mbarrier that never completes (bounded).
 cudaError_t launch_watchdog_selftest(int* status, uint64_t limit_ns,

@@ -36,6 +36,8 @@ struct Workspace {
   size_t ws_floats = 0;
   int* counters = nullptr;
   size_t counters_len = 0;
+  float* tr = nullptr;   // row-major copies of transposed operands
+  size_t tr_floats = 0;
 };
 
 struct DeviceState {
@@ -147,6 +149,18 @@ int ensure_workspace(DeviceState& st, cudaStream_t s, size_t floats,
   return SGEMM_OK;
 }
 
+// Grow the transposed-copy buffer of stream s's workspace (lock held).
+int ensure_tr(Workspace& w, size_t floats) {
+  if (floats <= w.tr_floats) return SGEMM_OK;
+  if (w.tr != nullptr) cudaFree(w.tr);
+  w.tr = nullptr;
+  w.tr_floats = 0;
+  if (cudaMalloc(&w.tr, floats * sizeof(float)) != cudaSuccess)
+    return SGEMM_ERR_CUDA;
+  w.tr_floats = floats;
+  return SGEMM_OK;
+}
+
 int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                const void* B, int64_t ldb, const void* C, int64_t ldc) {
   if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
@@ -179,30 +193,6 @@ bool overlaps(uint64_t a, int64_t ar, int64_t ac, int64_t ald, uint64_t c,
 bool tma_operand_ok(uint64_t addr, int64_t ld) {
   // TMA: 16-byte aligned base, row stride a multiple of 16 bytes and < 2^40.
   return addr % 16 == 0 && (ld * 4) % 16 == 0 && ld * 4 < (int64_t(1) << 40);
-}
-
-// Host-only path choice (no device access).
-int plan_path(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-              uint64_t a, uint64_t b) {
-  if (M == 0 || N == 0 || K == 0) return SGEMM_PATH_AUTO;  // no kernel
-  if (M == 1) return SGEMM_PATH_GEMV_ROW;
-  if (N == 1) return SGEMM_PATH_GEMV_COL;
-  // The stream-K schedule counts k-slice iterations in 32 bits.
-  const int64_t iters = ((M + kTileM - 1) / kTileM) *
-                        ((N + kTileN - 1) / kTileN) *
-                        ((K + kTileK - 1) / kTileK);
-  if (tma_operand_ok(a, lda) && tma_operand_ok(b, ldb) && iters < (1ll << 31)) {
-    const int64_t tiles = ((M + kTileM - 1) / kTileM) *
-                          ((N + kTileN - 1) / kTileN);
-    if (g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO &&
-        !(tiles < kTf32MinTiles && K >= kTf32LongK)) {
-      const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-      return pair_tiles >= kTf32PairMinTiles ? SGEMM_PATH_TF32X3_PAIR
-                                             : SGEMM_PATH_TF32X3;
-    }
-    return SGEMM_PATH_TILED_TMA;
-  }
-  return SGEMM_PATH_TILED_LDG;
 }
 
 int encode_maps(const GemmArgs& g, CUtensorMap* tmA, CUtensorMap* tmB) {
@@ -314,14 +304,25 @@ int to_status(cudaError_t e) {
              : SGEMM_ERR_CUDA;
 }
 
+// Maps of the tensor-core kernels. A K-major operand (A stored M x K, or B
+// stored N x K) is one box {32 k, 128 rows}; an MN-major one (A stored
+// K x M, or B stored K x N) is read as boxes {32 rows, 32 k}. All with the
+// 128-byte swizzle.
 int encode_tf32x3(const GemmArgs& g, CUtensorMap* tmA, CUtensorMap* tmB) {
-  const int rc = encode_2d(tmA, g.A, g.K, g.M, g.lda, 32, 128,
-                           CU_TENSOR_MAP_SWIZZLE_128B);
+  const int rc =
+      g.op_a == 0
+          ? encode_2d(tmA, g.A, g.K, g.M, g.lda, 32, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B)
+          : encode_2d(tmA, g.A, g.M, g.K, g.lda, 32, 32,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != SGEMM_OK) return rc;
-  return encode_2d(tmB, g.B, g.N, g.K, g.ldb, 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
+  return g.op_b == 0 ? encode_2d(tmB, g.B, g.N, g.K, g.ldb, 32, 32,
+                                 CU_TENSOR_MAP_SWIZZLE_128B)
+                     : encode_2d(tmB, g.B, g.K, g.N, g.ldb, 32, 128,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// (st.ws_mu held: the pair kernel uses the stream's workspace.)
 int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
                bool pair) {
   CUtensorMap tmA, tmB;
@@ -329,7 +330,6 @@ int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
   if (rc != SGEMM_OK) return rc;
   if (!pair) return to_status(launch_tf32x3(g, tmA, tmB, st.status, s));
   const PairPlan pl = plan_pair(g.M, g.N, g.K, st.pair_clusters, true);
-  std::lock_guard<std::mutex> lock(st.ws_mu);
   Workspace* w = nullptr;
   const int wrc = ensure_workspace(st, s, pl.ws_floats, pl.counters, &w);
   if (wrc != SGEMM_OK) return wrc;
@@ -337,43 +337,202 @@ int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
                                       st.status, s));
 }
 
-int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-        const float* B, int64_t ldb, float* C, int64_t ldc, void* stream,
-        int path) {
-  int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+// ---------------------------------------------------------------- calls
+//
+// Every computing entry point is one call C = alpha * op(A) * op(B) +
+// beta * C (sgemm: no transposes, alpha = 1, beta = 0).
+struct Call {
+  int op_a, op_b;
+  int64_t M, N, K;
+  float alpha;
+  const float* A;
+  int64_t lda;
+  const float* B;
+  int64_t ldb;
+  float beta;
+  float* C;
+  int64_t ldc;
+};
+
+// A and B are read only when there are products to form (BLAS: alpha == 0
+// leaves them unreferenced).
+bool reads_ab(const Call& c) { return c.alpha != 0.f && c.K > 0; }
+
+int check_call(const Call& c) {
+  if ((c.op_a != SGEMM_OP_N && c.op_a != SGEMM_OP_T) ||
+      (c.op_b != SGEMM_OP_N && c.op_b != SGEMM_OP_T))
+    return SGEMM_ERR_INVALID_VALUE;
+  if (c.M < 0 || c.N < 0 || c.K < 0) return SGEMM_ERR_INVALID_VALUE;
+  const int64_t a_cols = c.op_a ? c.M : c.K, b_cols = c.op_b ? c.K : c.N;
+  if (c.lda < (a_cols > 1 ? a_cols : 1) || c.ldb < (b_cols > 1 ? b_cols : 1) ||
+      c.ldc < (c.N > 1 ? c.N : 1))
+    return SGEMM_ERR_INVALID_VALUE;
+  if (c.M > kMaxDim || c.N > kMaxDim || c.K > kMaxDim)
+    return SGEMM_ERR_TOO_LARGE;
+  if (c.M > 0 && c.N > 0) {
+    if (c.C == nullptr) return SGEMM_ERR_NULL_POINTER;
+    if (reads_ab(c) && (c.A == nullptr || c.B == nullptr))
+      return SGEMM_ERR_NULL_POINTER;
+  }
+  return SGEMM_OK;
+}
+
+bool call_overlaps(const Call& c) {
+  if (!reads_ab(c)) return false;
+  const uint64_t a = reinterpret_cast<uint64_t>(c.A);
+  const uint64_t b = reinterpret_cast<uint64_t>(c.B);
+  const uint64_t cc = reinterpret_cast<uint64_t>(c.C);
+  return overlaps(a, c.op_a ? c.K : c.M, c.op_a ? c.M : c.K, c.lda, cc, c.M,
+                  c.N, c.ldc) ||
+         overlaps(b, c.op_b ? c.N : c.K, c.op_b ? c.K : c.N, c.ldb, cc, c.M,
+                  c.N, c.ldc);
+}
+
+// Host-only path choice (no device access): the kernel that computes the
+// products. AUTO when no kernel runs (empty C, or nothing to multiply).
+int plan_call(const Call& c) {
+  if (c.M == 0 || c.N == 0 || !reads_ab(c)) return SGEMM_PATH_AUTO;
+  const uint64_t a = reinterpret_cast<uint64_t>(c.A);
+  const uint64_t b = reinterpret_cast<uint64_t>(c.B);
+  // c = a * B^T is a product of B's rows with a: the N == 1 kernel.
+  if (c.M == 1) return c.op_b ? SGEMM_PATH_GEMV_COL : SGEMM_PATH_GEMV_ROW;
+  if (c.N == 1) return SGEMM_PATH_GEMV_COL;
+  const int64_t tiles = ((c.M + kTileM - 1) / kTileM) *
+                        ((c.N + kTileN - 1) / kTileN);
+  if (tma_operand_ok(a, c.lda) && tma_operand_ok(b, c.ldb) &&
+      g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO &&
+      !(tiles < kTf32MinTiles && c.K >= kTf32LongK)) {
+    const int64_t pair_tiles = ((c.M + 255) / 256) * ((c.N + 255) / 256);
+    return pair_tiles >= kTf32PairMinTiles ? SGEMM_PATH_TF32X3_PAIR
+                                           : SGEMM_PATH_TF32X3;
+  }
+  // CUDA-core tile kernels take row-major operands; a transposed one is
+  // first copied row-major (dense, ld = its width) into the workspace.
+  const bool a_ok = c.op_a ? c.K % 4 == 0 : tma_operand_ok(a, c.lda);
+  const bool b_ok = c.op_b ? c.N % 4 == 0 : tma_operand_ok(b, c.ldb);
+  // The stream-K schedule counts k-slice iterations in 32 bits.
+  const int64_t iters = tiles * ((c.K + kTileK - 1) / kTileK);
+  return a_ok && b_ok && iters < (1ll << 31) ? SGEMM_PATH_TILED_TMA
+                                             : SGEMM_PATH_TILED_LDG;
+}
+
+int plan_path(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              uint64_t a, uint64_t b) {
+  const Call c{SGEMM_OP_N, SGEMM_OP_N, M, N, K, 1.f,
+               reinterpret_cast<const float*>(a), lda,
+               reinterpret_cast<const float*>(b), ldb, 0.f, nullptr, 1};
+  return plan_call(c);
+}
+
+// Replace transposed operands of g by row-major copies in the workspace of
+// stream s (st.ws_mu held): op(A) as M x K (ld K), op(B) as K x N (ld N).
+int make_row_major(GemmArgs& g, DeviceState& st, cudaStream_t s) {
+  if (!g.op_a && !g.op_b) return SGEMM_OK;
+  const size_t a_floats = g.op_a ? size_t(g.M) * size_t(g.K) : 0;
+  const size_t a_pad = (a_floats + 63) / 64 * 64;  // B copy 256-byte aligned
+  const size_t b_floats = g.op_b ? size_t(g.K) * size_t(g.N) : 0;
+  Workspace* w = nullptr;
+  int rc = ensure_workspace(st, s, 0, 0, &w);
+  if (rc == SGEMM_OK) rc = ensure_tr(*w, a_pad + b_floats);
+  if (rc != SGEMM_OK) return rc;
+  if (g.op_a) {  // A stored K x M -> M x K
+    rc = to_status(launch_transpose(g.A, g.lda, g.K, g.M, w->tr, s));
+    if (rc != SGEMM_OK) return rc;
+    g.A = w->tr;
+    g.lda = g.K > 1 ? g.K : 1;
+    g.op_a = 0;
+  }
+  if (g.op_b) {  // B stored N x K -> K x N
+    rc = to_status(launch_transpose(g.B, g.ldb, g.N, g.K, w->tr + a_pad, s));
+    if (rc != SGEMM_OK) return rc;
+    g.B = w->tr + a_pad;
+    g.ldb = g.N > 1 ? g.N : 1;
+    g.op_b = 0;
+  }
+  return SGEMM_OK;
+}
+
+int run_call(const Call& call, void* stream, int path) {
+  int rc = check_call(call);
   if (rc != SGEMM_OK) return rc;
   if (path < 0 || path >= SGEMM_PATH_COUNT) return SGEMM_ERR_INVALID_VALUE;
-  if (M == 0 || N == 0) return SGEMM_OK;
-  const uint64_t a = reinterpret_cast<uint64_t>(A);
-  const uint64_t b = reinterpret_cast<uint64_t>(B);
-  const uint64_t c = reinterpret_cast<uint64_t>(C);
-  if (K > 0 && (overlaps(a, M, K, lda, c, M, N, ldc) ||
-                overlaps(b, K, N, ldb, c, M, N, ldc)))
-    return SGEMM_ERR_OVERLAP;
+  if (call.M == 0 || call.N == 0) return SGEMM_OK;
+  if (call_overlaps(call)) return SGEMM_ERR_OVERLAP;
 
   DeviceState* st = nullptr;
   rc = device_state(&st);
   if (rc != SGEMM_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  if (K == 0)  // empty sum
-    return to_status(cudaMemset2DAsync(C, size_t(ldc) * 4, 0, size_t(N) * 4,
-                                       size_t(M), s));
+  if (!reads_ab(call)) {  // empty sum or alpha == 0: C = beta * C
+    if (call.beta == 1.f) return SGEMM_OK;
+    if (call.beta == 0.f)
+      return to_status(cudaMemset2DAsync(call.C, size_t(call.ldc) * 4, 0,
+                                         size_t(call.N) * 4, size_t(call.M),
+                                         s));
+    return to_status(
+        launch_scale_c(call.C, call.ldc, call.M, call.N, call.beta, s));
+  }
 
-  if (path == SGEMM_PATH_AUTO) path = plan_path(M, N, K, lda, ldb, a, b);
-  const GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc};
+  if (path == SGEMM_PATH_AUTO) path = plan_call(call);
+  GemmArgs g{call.M,   call.N, call.K,   call.A, call.lda,
+             call.B,   call.ldb, call.C, call.ldc};
+  g.sc.alpha = call.alpha;
+  g.sc.beta = call.beta;
+  g.op_a = call.op_a;
+  g.op_b = call.op_b;
+  const uint64_t a = reinterpret_cast<uint64_t>(call.A);
+  const uint64_t b = reinterpret_cast<uint64_t>(call.B);
+  std::lock_guard<std::mutex> lock(st->ws_mu);  // workspace of stream s
   switch (path) {
-    case SGEMM_PATH_TILED_TMA: {
-      if (!tma_operand_ok(a, lda) || !tma_operand_ok(b, ldb))
+    case SGEMM_PATH_TF32X3:
+    case SGEMM_PATH_TF32X3_PAIR:
+      if (!tma_operand_ok(a, call.lda) || !tma_operand_ok(b, call.ldb))
         return SGEMM_ERR_PATH;
-      if (plan_stream_k(M, N, K, 1).total_iters >= (1ll << 31))
+      return run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR);
+    case SGEMM_PATH_GEMV_COL: {
+      if (call.M == 1 && call.N != 1 && call.op_b) {
+        // c = op(a) * B^T: row j of B (stored N x K) times the vector a
+        // (A's row, or its column with stride lda when stored K x 1).
+        GemmArgs h{call.N, 1, call.K, call.B, call.ldb, call.A,
+                   call.op_a ? call.lda : 1, call.C, 1};
+        h.sc = g.sc;
+        const cudaError_t e = run_gemv_col(h, *st, s, &rc);
+        return rc != SGEMM_OK ? rc : to_status(e);
+      }
+      if (call.N != 1) return SGEMM_ERR_PATH;
+      if (g.op_a) {
+        g.op_b = 0;  // B's column is read with its own stride below
+        g.op_a = 1;
+        rc = make_row_major(g, *st, s);
+        if (rc != SGEMM_OK) return rc;
+      }
+      // the vector b = op(B)'s column: stride ldb (stored K x 1) or 1
+      g.ldb = call.op_b ? 1 : call.ldb;
+      g.op_b = 0;
+      const cudaError_t e = run_gemv_col(g, *st, s, &rc);
+      return rc != SGEMM_OK ? rc : to_status(e);
+    }
+    case SGEMM_PATH_GEMV_ROW: {
+      if (call.M != 1) return SGEMM_ERR_PATH;
+      rc = make_row_major(g, *st, s);
+      if (rc != SGEMM_OK) return rc;
+      const cudaError_t e = run_gemv_row(g, *st, s, &rc);
+      return rc != SGEMM_OK ? rc : to_status(e);
+    }
+    case SGEMM_PATH_TILED_TMA: {
+      rc = make_row_major(g, *st, s);
+      if (rc != SGEMM_OK) return rc;
+      if (!tma_operand_ok(reinterpret_cast<uint64_t>(g.A), g.lda) ||
+          !tma_operand_ok(reinterpret_cast<uint64_t>(g.B), g.ldb))
+        return SGEMM_ERR_PATH;
+      if (plan_stream_k(g.M, g.N, g.K, 1).total_iters >= (1ll << 31))
         return SGEMM_ERR_TOO_LARGE;
       CUtensorMap tmA, tmB;
       rc = encode_maps(g, &tmA, &tmB);
       if (rc != SGEMM_OK) return rc;
       const SkPlan pl =
-          plan_stream_k(M, N, K, st->sms * st->tma_blocks_per_sm);
-      std::lock_guard<std::mutex> lock(st->ws_mu);
+          plan_stream_k(g.M, g.N, g.K, st->sms * st->tma_blocks_per_sm);
       Workspace* w = nullptr;
       rc = ensure_workspace(*st, s, pl.ws_floats, size_t(pl.tiles), &w);
       if (rc != SGEMM_OK) return rc;
@@ -381,27 +540,24 @@ int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                         st->status, s));
     }
     case SGEMM_PATH_TILED_LDG:
+      rc = make_row_major(g, *st, s);
+      if (rc != SGEMM_OK) return rc;
       return to_status(launch_tiled_ldg(g, st->status, s));
-    case SGEMM_PATH_GEMV_ROW: {
-      if (M != 1) return SGEMM_ERR_PATH;
-      const cudaError_t e = run_gemv_row(g, *st, s, &rc);
-      return rc != SGEMM_OK ? rc : to_status(e);
-    }
-    case SGEMM_PATH_GEMV_COL: {
-      if (N != 1) return SGEMM_ERR_PATH;
-      const cudaError_t e = run_gemv_col(g, *st, s, &rc);
-      return rc != SGEMM_OK ? rc : to_status(e);
-    }
     case SGEMM_PATH_NAIVE:
+      rc = make_row_major(g, *st, s);
+      if (rc != SGEMM_OK) return rc;
       return to_status(launch_naive(g, s));
-    case SGEMM_PATH_TF32X3:
-    case SGEMM_PATH_TF32X3_PAIR:
-      if (!tma_operand_ok(a, lda) || !tma_operand_ok(b, ldb))
-        return SGEMM_ERR_PATH;
-      return run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR);
     default:
       return SGEMM_ERR_PATH;
   }
+}
+
+int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+        const float* B, int64_t ldb, float* C, int64_t ldc, void* stream,
+        int path) {
+  const Call c{SGEMM_OP_N, SGEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f,
+               C, ldc};
+  return run_call(c, stream, path);
 }
 
 }  // namespace
@@ -602,6 +758,35 @@ int sgemm_path(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                const float* B, int64_t ldb, float* C, int64_t ldc,
                void* stream, int path) {
   return dfm::run(M, N, K, A, lda, B, ldb, C, ldc, stream, path);
+}
+
+int sgemm_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+             float alpha, const float* A, int64_t lda, const float* B,
+             int64_t ldb, float beta, float* C, int64_t ldc, void* stream) {
+  const dfm::Call c{op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc};
+  return dfm::run_call(c, stream, SGEMM_PATH_AUTO);
+}
+
+int sgemm_ex_path(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                  float alpha, const float* A, int64_t lda, const float* B,
+                  int64_t ldb, float beta, float* C, int64_t ldc, void* stream,
+                  int path) {
+  const dfm::Call c{op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc};
+  return dfm::run_call(c, stream, path);
+}
+
+int sgemm_plan_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc, uint64_t a_addr,
+                  uint64_t b_addr, uint64_t c_addr, int* path) {
+  if (path == nullptr) return SGEMM_ERR_NULL_POINTER;
+  const dfm::Call c{op_a, op_b, M, N, K, 1.f,
+                    reinterpret_cast<const float*>(a_addr), lda,
+                    reinterpret_cast<const float*>(b_addr), ldb, 0.f,
+                    reinterpret_cast<float*>(c_addr), ldc};
+  const int rc = dfm::check_call(c);
+  if (rc != SGEMM_OK) return rc;
+  *path = dfm::plan_call(c);
+  return SGEMM_OK;
 }
 
 int sgemm_set_math_mode(int mode) {

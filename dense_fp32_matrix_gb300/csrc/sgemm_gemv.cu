@@ -42,7 +42,8 @@ constexpr size_t GR_SMEM =
 __global__ void __launch_bounds__(kThreads)
 k_gemv_row_tma(const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tma_, float* __restrict__ c,
-               int N, int K, int k_per_block, int cluster, int* status) {
+               int N, int K, int k_per_block, int cluster, Scale sc,
+               int* status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ float red[GR_GROUPS][GR_COLS];
   __shared__ float part[GR_MAX_CLUSTER][GR_COLS];  // used in rank 0
@@ -118,7 +119,8 @@ k_gemv_row_tma(const __grid_constant__ CUtensorMap tmB,
     for (int q = 0; q < GR_GROUPS; ++q) s += red[q][tid];
   }
   if (cluster == 1) {
-    if (tid < GR_COLS && !aborted && n0 + tid < N) c[n0 + tid] = s;
+    if (tid < GR_COLS && !aborted && n0 + tid < N)
+      c[n0 + tid] = epi1(s, c + n0 + tid, sc);
     return;
   }
   // Rank r's 64 partials go to slot r of rank 0's buffer; rank 0 adds the
@@ -130,7 +132,7 @@ k_gemv_row_tma(const __grid_constant__ CUtensorMap tmB,
   if (rank == 0 && tid < GR_COLS && !aborted && n0 + tid < N) {
     float total = 0.f;
     for (int q = 0; q < cluster; ++q) total += part[q][tid];
-    c[n0 + tid] = total;
+    c[n0 + tid] = epi1(total, c + n0 + tid, sc);
   }
 }
 
@@ -148,7 +150,7 @@ static_assert(GC_K / 4 == 4 * GC_LANES, "4 float4 per lane per stage");
 __global__ void __launch_bounds__(kThreads)
 k_gemv_col_tma(const __grid_constant__ CUtensorMap tmA,
                const __grid_constant__ CUtensorMap tmb, float* __restrict__ c,
-               long long ldc, int M, int K, int* status) {
+               long long ldc, int M, int K, Scale sc, int* status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sA = smem_raw + (((raw + 127u) & ~127u) - raw);
@@ -210,7 +212,8 @@ k_gemv_col_tma(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
   for (int off = GC_LANES / 2; off > 0; off >>= 1)
     acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (s == 0 && m0 + r < M) c[(long long)(m0 + r) * ldc] = acc;
+  if (s == 0 && m0 + r < M)
+    c[(long long)(m0 + r) * ldc] = epi1(acc, c + (long long)(m0 + r) * ldc, sc);
 }
 
 }  // namespace
@@ -257,7 +260,8 @@ cudaError_t launch_gemv_row_tma(const GemmArgs& g, const CUtensorMap& tmB,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_gemv_row_tma, tmB, tma_, g.C, int(g.N),
-                            int(g.K), int(pl.k_per_block), pl.cluster, status);
+                            int(g.K), int(pl.k_per_block), pl.cluster, g.sc,
+                            status);
 }
 
 cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
@@ -265,7 +269,7 @@ cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
                                 cudaStream_t s) {
   const unsigned blocks = unsigned((g.M + GC_ROWS - 1) / GC_ROWS);
   k_gemv_col_tma<<<blocks, kThreads, GC_SMEM, s>>>(
-      tmA, tmb, g.C, (long long)g.ldc, int(g.M), int(g.K), status);
+      tmA, tmb, g.C, (long long)g.ldc, int(g.M), int(g.K), g.sc, status);
   return cudaGetLastError();
 }
 

@@ -29,7 +29,7 @@ constexpr int ROW_UNROLL = 8;
 template <bool VEC>
 __global__ void __launch_bounds__(ROW_THREADS)
 k_gemv_row(const float* __restrict__ a, const float* __restrict__ B,
-           long long ldb, float* __restrict__ c, int N, int K) {
+           long long ldb, float* __restrict__ c, int N, int K, Scale sc) {
   __shared__ float part[ROW_GROUPS][ROW_COLS + 1];
   const int tid = threadIdx.x;
   const int grp = tid >> 2, q = tid & 3;
@@ -89,7 +89,7 @@ k_gemv_row(const float* __restrict__ a, const float* __restrict__ B,
     const int j = blockIdx.x * ROW_COLS + tid;
     float s = 0.f;
     for (int g = 0; g < ROW_GROUPS; ++g) s += part[g][tid];
-    if (j < N) c[j] = s;
+    if (j < N) c[j] = epi1(s, c + j, sc);
   }
 }
 
@@ -99,7 +99,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(COL_WARPS * 32)
 k_gemv_col(const float* __restrict__ A, long long lda,
            const float* __restrict__ b, long long ldb, float* __restrict__ c,
-           long long ldc, int M, int K) {
+           long long ldc, int M, int K, Scale sc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = blockIdx.x * COL_WARPS + warp; i < M;
        i += gridDim.x * COL_WARPS) {
@@ -142,14 +142,14 @@ k_gemv_col(const float* __restrict__ A, long long lda,
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
       acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) c[(long long)i * ldc] = acc;
+    if (lane == 0) c[(long long)i * ldc] = epi1(acc, c + (long long)i * ldc, sc);
   }
 }
 
 __global__ void k_naive(const float* __restrict__ A, long long lda,
                         const float* __restrict__ B, long long ldb,
                         float* __restrict__ C, long long ldc, int M, int N,
-                        int K) {
+                        int K, Scale sc) {
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   for (int i = blockIdx.y * blockDim.y + threadIdx.y; i < M;
        i += gridDim.y * blockDim.y) {
@@ -157,7 +157,48 @@ __global__ void k_naive(const float* __restrict__ A, long long lda,
     float acc = 0.f;
     for (int k = 0; k < K; ++k)
       acc = fmaf(A[(long long)i * lda + k], B[(long long)k * ldb + j], acc);
-    C[(long long)i * ldc + j] = acc;
+    C[(long long)i * ldc + j] = epi1(acc, C + (long long)i * ldc + j, sc);
+  }
+}
+
+// out (cols x rows, dense) = in (rows x cols, ld) transposed. 32 x 32
+// tiles through shared memory (one padding column: conflict-free), so both
+// the reads and the writes are coalesced rows.
+constexpr int TR_TILE = 32, TR_ROWS = 8;
+
+__global__ void __launch_bounds__(TR_TILE * TR_ROWS)
+k_transpose(const float* __restrict__ in, long long ld, int rows, int cols,
+            float* __restrict__ out) {
+  __shared__ float t[TR_TILE][TR_TILE + 1];
+  const int c0 = blockIdx.x * TR_TILE;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (long long r0 = (long long)blockIdx.y * TR_TILE; r0 < rows;
+       r0 += (long long)gridDim.y * TR_TILE) {
+#pragma unroll
+    for (int k = 0; k < TR_TILE; k += TR_ROWS) {
+      const long long r = r0 + ty + k;
+      const int c = c0 + tx;
+      if (r < rows && c < cols) t[ty + k][tx] = in[r * ld + c];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < TR_TILE; k += TR_ROWS) {
+      const int c = c0 + ty + k;
+      const long long r = r0 + tx;
+      if (r < rows && c < cols) out[(long long)c * rows + r] = t[tx][ty + k];
+    }
+    __syncthreads();  // t is refilled by the next row tile
+  }
+}
+
+// C = beta * C (beta == 0: C = 0 without reading it).
+__global__ void k_scale_c(float* __restrict__ C, long long ldc, int M, int N,
+                          float beta) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= N) return;
+  for (int i = blockIdx.y; i < M; i += gridDim.y) {
+    float* c = C + (long long)i * ldc + j;
+    *c = beta == 0.f ? 0.f : beta * *c;
   }
 }
 
@@ -188,10 +229,10 @@ cudaError_t launch_gemv_row(const GemmArgs& g, int num_sms, cudaStream_t s) {
   const unsigned blocks = unsigned((g.N + ROW_COLS - 1) / ROW_COLS);
   if (vec)
     k_gemv_row<true><<<blocks, ROW_THREADS, 0, s>>>(g.A, g.B, g.ldb, g.C,
-                                                     int(g.N), int(g.K));
+                                                     int(g.N), int(g.K), g.sc);
   else
     k_gemv_row<false><<<blocks, ROW_THREADS, 0, s>>>(g.A, g.B, g.ldb, g.C,
-                                                      int(g.N), int(g.K));
+                                                      int(g.N), int(g.K), g.sc);
   return cudaGetLastError();
 }
 
@@ -204,10 +245,10 @@ cudaError_t launch_gemv_col(const GemmArgs& g, int num_sms, cudaStream_t s) {
   if (blocks > cap) blocks = cap;
   if (vec)
     k_gemv_col<true><<<unsigned(blocks), COL_WARPS * 32, 0, s>>>(
-        g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M), int(g.K));
+        g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M), int(g.K), g.sc);
   else
     k_gemv_col<false><<<unsigned(blocks), COL_WARPS * 32, 0, s>>>(
-        g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M), int(g.K));
+        g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M), int(g.K), g.sc);
   return cudaGetLastError();
 }
 
@@ -217,7 +258,27 @@ cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s) {
   if (gy > 65535) gy = 65535;
   const dim3 grid(unsigned((g.N + 31) / 32), unsigned(gy));
   k_naive<<<grid, block, 0, s>>>(g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M),
-                                 int(g.N), int(g.K));
+                                 int(g.N), int(g.K), g.sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const float* in, int64_t ld, int64_t rows,
+                             int64_t cols, float* out, cudaStream_t s) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int64_t row_tiles = (rows + TR_TILE - 1) / TR_TILE;
+  const dim3 grid(unsigned((cols + TR_TILE - 1) / TR_TILE),
+                  unsigned(row_tiles < 65535 ? row_tiles : 65535));
+  k_transpose<<<grid, dim3(TR_TILE, TR_ROWS), 0, s>>>(in, (long long)ld,
+                                                      int(rows), int(cols), out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_c(float* C, int64_t ldc, int64_t M, int64_t N,
+                           float beta, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  long long gy = M < 65535 ? M : 65535;
+  k_scale_c<<<dim3(unsigned((N + 255) / 256), unsigned(gy)), 256, 0, s>>>(
+      C, (long long)ldc, int(M), int(N), beta);
   return cudaGetLastError();
 }
 

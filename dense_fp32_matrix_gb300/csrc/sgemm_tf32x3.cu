@@ -171,6 +171,77 @@ __device__ __forceinline__ void split_transpose_half(uint8_t* box,
   }
 }
 
+// ------------------------------------------------- operand layouts (op)
+//
+// Both MMA operands must be K-major (reading 14 of the design notes). Per
+// operand the stored layout decides the work:
+//   A, op_a == 0 (stored M x K) and B, op_b == 1 (stored N x K): K-major
+//     already; one TMA box {32 k, 128 rows} lands in the canonical
+//     128-byte-swizzled layout and only the low part is split off.
+//   A, op_a == 1 (stored K x M) and B, op_b == 0 (stored K x N): MN-major;
+//     four boxes {32 rows, 32 k} land N-major and are transposed in place
+//     into K-major rows (split_transpose_box / _half).
+// (128-row halves: the 1-SM kernel's tile and each block's half of a pair.)
+template <int OA, int OB>
+__device__ __forceinline__ void load_stage(uint8_t* a_buf, uint8_t* b_buf,
+                                           const CUtensorMap* tmA,
+                                           const CUtensorMap* tmB, int k,
+                                           int m0, int n0, uint32_t bar) {
+  if (OA == 0) {
+    tma_load_2d(smem_u32(a_buf), tmA, k * XK, m0, bar);
+  } else {
+    for (int j = 0; j < 4; ++j)
+      tma_load_2d(smem_u32(a_buf + j * X_B_BOX), tmA, m0 + 32 * j, k * XK,
+                  bar);
+  }
+  if (OB == 0) {
+    for (int j = 0; j < 4; ++j)
+      tma_load_2d(smem_u32(b_buf + j * X_B_BOX), tmB, n0 + 32 * j, k * XK,
+                  bar);
+  } else {
+    tma_load_2d(smem_u32(b_buf), tmB, k * XK, n0, bar);
+  }
+}
+
+template <int OA, int OB>
+__device__ __forceinline__ void prefetch_stage(const CUtensorMap* tmA,
+                                               const CUtensorMap* tmB, int k,
+                                               int m0, int n0) {
+  if (OA == 0) {
+    tma_prefetch_l2_2d(tmA, k * XK, m0);
+  } else {
+    for (int j = 0; j < 4; ++j) tma_prefetch_l2_2d(tmA, m0 + 32 * j, k * XK);
+  }
+  if (OB == 0) {
+    for (int j = 0; j < 4; ++j) tma_prefetch_l2_2d(tmB, n0 + 32 * j, k * XK);
+  } else {
+    tma_prefetch_l2_2d(tmB, k * XK, n0);
+  }
+}
+
+// 1-SM kernel: 4 split warps (w = 0..3, ct = 0..127). K-major operands are
+// split elementwise by all of them (hi masked in place, lo beside), an
+// MN-major operand box by box, one box per warp.
+template <int OA, int OB>
+__device__ __forceinline__ void split_stage_1sm(uint8_t* A, uint8_t* Alo,
+                                                uint8_t* B, uint8_t* Blo,
+                                                int w, int lane, int ct) {
+  if (OA == 0) {
+#pragma unroll
+    for (int q = 0; q < X_A_BYTES / 16 / X_CONV_THREADS; ++q)
+      split4(A, Alo, ct + X_CONV_THREADS * q);
+  } else {
+    split_transpose_box(A + w * X_B_BOX, Alo + w * X_B_BOX, lane);
+  }
+  if (OB == 0) {
+    split_transpose_box(B + w * X_B_BOX, Blo + w * X_B_BOX, lane);
+  } else {
+#pragma unroll
+    for (int q = 0; q < X_B_BYTES / 16 / X_CONV_THREADS; ++q)
+      split4(B, Blo, ct + X_CONV_THREADS * q);
+  }
+}
+
 __device__ __forceinline__ void tile_of(int tile, int tiles_m, int tiles_n,
                                         int& pm, int& pn) {
   const int per_group = X_GROUP_M * tiles_n;
@@ -182,11 +253,12 @@ __device__ __forceinline__ void tile_of(int tile, int tiles_m, int tiles_n,
   pn = in_group / rows;
 }
 
+template <int OA, int OB>
 __global__ void __launch_bounds__(X_THREADS, 1)
 k_tf32x3(const __grid_constant__ CUtensorMap tmA,
          const __grid_constant__ CUtensorMap tmB, float* __restrict__ C, int M,
          int N, int K, long long ldc, int tiles_m, int tiles_n, int vec_store,
-         int* status) {
+         Scale sc, int* status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -244,10 +316,7 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
         }
         const uint32_t bar = full0 + 8 * s;
         mbar_arrive_expect_tx(bar, X_A_BYTES + X_B_BYTES);
-        tma_load_2d(smem_u32(A_of(s)), &tmA, t * XK, m0, bar);
-        for (int j = 0; j < XN / 32; ++j)
-          tma_load_2d(smem_u32(B_of(s) + j * X_B_BOX), &tmB, n0 + 32 * j,
-                      t * XK, bar);
+        load_stage<OA, OB>(A_of(s), B_of(s), &tmA, &tmB, t, m0, n0, bar);
       }
     }
   } else if (warp == 1) {
@@ -296,12 +365,8 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
         *abort_flag = 1;
         break;
       }
-#pragma unroll
-      for (int q = 0; q < X_A_BYTES / 16 / X_CONV_THREADS; ++q)
-        split4(A_of(s), Alo_of(s), ct + X_CONV_THREADS * q);
-      // warp w - 2 owns B box w - 2 (columns 32 (w - 2) .. + 31)
-      split_transpose_box(B_of(s) + (warp - 2) * X_B_BOX,
-                          Blo_of(s) + (warp - 2) * X_B_BOX, lane);
+      split_stage_1sm<OA, OB>(A_of(s), Alo_of(s), B_of(s), Blo_of(s), warp - 2,
+                              lane, ct);
       fence_async_shared();  // generic writes -> visible to the MMA
       __syncwarp();
       if (lane == 0) mbar_arrive(conv0 + 8 * s);
@@ -326,13 +391,15 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
       for (int e = 0; e < 32; e += 4) {
         const int c = c0 + e;
         if (vec_store && c + 3 < N) {
-          *reinterpret_cast<float4*>(crow + c) =
+          *reinterpret_cast<float4*>(crow + c) = epi4(
               make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                          __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                          __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])),
+              crow + c, sc);
         } else {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            if (c + u < N) crow[c + u] = __uint_as_float(v[e + u]);
+            if (c + u < N)
+              crow[c + u] = epi1(__uint_as_float(v[e + u]), crow + c + u, sc);
         }
       }
     }
@@ -403,8 +470,42 @@ struct PairParams {
   float* ws;            // 2 pieces per block: G x 2 x 2 x P_PIECE_FLOATS
   int* counters;        // sk_tiles x 2 blocks x 4 quarters, zero between calls
   int vec_store;
+  Scale sc;
   int* status;
 };
+
+// Pair kernel: 8 split warps (cw = 0..7, ct = 0..255). K-major operands:
+// the landed tile is the high part, all threads write the low part. One
+// MN-major operand: two warps per box, one per 16-k half. Both MN-major:
+// one box per warp.
+template <int OA, int OB>
+__device__ __forceinline__ void split_stage_pair(uint8_t* A, uint8_t* Alo,
+                                                 uint8_t* B, uint8_t* Blo,
+                                                 int cw, int lane, int ct) {
+  constexpr int kThreads = 256;
+  const int box = cw >> 1, half = cw & 1, bar_id = 1 + box;
+  if (OA == 0) {
+#pragma unroll
+    for (int q = 0; q < X_A_BYTES / 16 / kThreads; ++q)
+      split4_lo(A, Alo, ct + kThreads * q);
+  }
+  if (OB == 1) {
+#pragma unroll
+    for (int q = 0; q < X_B_BYTES / 16 / kThreads; ++q)
+      split4_lo(B, Blo, ct + kThreads * q);
+  }
+  if (OA == 1 && OB == 0) {
+    uint8_t* x = cw < 4 ? A : B;
+    uint8_t* lo = cw < 4 ? Alo : Blo;
+    split_transpose_box(x + (cw & 3) * X_B_BOX, lo + (cw & 3) * X_B_BOX, lane);
+  } else if (OA == 1) {
+    split_transpose_half(A + box * X_B_BOX, Alo + box * X_B_BOX, lane, half,
+                         bar_id);
+  } else if (OB == 0) {
+    split_transpose_half(B + box * X_B_BOX, Blo + box * X_B_BOX, lane, half,
+                         bar_id);
+  }
+}
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile(
@@ -486,18 +587,21 @@ __device__ __forceinline__ void store_c_quarter(uint32_t acc, float* crow,
     for (int e = 0; e < 32; e += 4) {
       const int c = c0 + e;
       if (p.vec_store && c + 3 < p.N) {
-        *reinterpret_cast<float4*>(crow + c) =
+        *reinterpret_cast<float4*>(crow + c) = epi4(
             make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])),
+            crow + c, p.sc);
       } else {
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          if (c + u < p.N) crow[c + u] = __uint_as_float(v[e + u]);
+          if (c + u < p.N)
+            crow[c + u] = epi1(__uint_as_float(v[e + u]), crow + c + u, p.sc);
       }
     }
   }
 }
 
+template <int OA, int OB>
 __global__ void __launch_bounds__(P_THREADS, 1)
 k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
               const __grid_constant__ CUtensorMap tmB, const PairParams p) {
@@ -572,17 +676,12 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
           }
           const uint32_t bar = full0 + 8 * s;
           mbar_arrive_expect_tx(bar, X_A_BYTES + X_B_BYTES);
-          tma_load_2d(smem_u32(A_of(s)), &tmA, k * XK, m_own, bar);
-          for (int j = 0; j < 128 / 32; ++j)
-            tma_load_2d(smem_u32(B_of(s) + j * X_B_BOX), &tmB, n_own + 32 * j,
-                        k * XK, bar);
+          load_stage<OA, OB>(A_of(s), B_of(s), &tmA, &tmB, k, m_own, n_own,
+                             bar);
           // warm L2 with the tiles of a later k-slice of this unit, so that
           // its load (issued when a stage frees up) is an L2 hit
-          if (k + P_PREFETCH < w.ke) {
-            tma_prefetch_l2_2d(&tmA, (k + P_PREFETCH) * XK, m_own);
-            for (int j = 0; j < 128 / 32; ++j)
-              tma_prefetch_l2_2d(&tmB, n_own + 32 * j, (k + P_PREFETCH) * XK);
-          }
+          if (k + P_PREFETCH < w.ke)
+            prefetch_stage<OA, OB>(&tmA, &tmB, k + P_PREFETCH, m_own, n_own);
         }
       }
       // Let the last loads land before the block can exit (they complete
@@ -674,8 +773,8 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
   } else if (warp < P_EPI_WARP0) {
     // ---------------------------------------------------------- split
     const int ct = tid - 64;  // 0..255
-    const int box = (warp - 2) >> 1, half = (warp - 2) & 1;
-    const int bar_id = 1 + box;  // named barrier of this box's two warps
+    // named barrier of warps 2c and 2c + 1 (they may share a B box)
+    const int bar_id = 1 + ((warp - 2) >> 1);
     int g = 0;
     bool ok = true;
     Unit w;
@@ -692,11 +791,8 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
           *abort_flag = 1;
           break;
         }
-#pragma unroll
-        for (int q = 0; q < X_A_BYTES / 16 / P_CONV_THREADS; ++q)
-          split4_lo(A_of(s), Alo_of(s), ct + P_CONV_THREADS * q);
-        split_transpose_half(B_of(s) + box * X_B_BOX,
-                             Blo_of(s) + box * X_B_BOX, lane, half, bar_id);
+        split_stage_pair<OA, OB>(A_of(s), Alo_of(s), B_of(s), Blo_of(s),
+                                 warp - 2, lane, ct);
         fence_async_shared();  // generic writes -> visible to the MMA
         __syncwarp();
         if (lane == 0) mbar_arrive(conv0 + 8 * s);
@@ -797,12 +893,12 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
         for (int e = 0; e < 8; ++e) {
           const int c = c0 + 4 * e;
           if (p.vec_store && c + 3 < p.N) {
-            *reinterpret_cast<float4*>(crow + c) = sum[e];
+            *reinterpret_cast<float4*>(crow + c) = epi4(sum[e], crow + c, p.sc);
           } else {
             const float s4[4] = {sum[e].x, sum[e].y, sum[e].z, sum[e].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              if (c + q < p.N) crow[c + q] = s4[q];
+              if (c + q < p.N) crow[c + q] = epi1(s4[q], crow + c + q, p.sc);
           }
         }
       }
@@ -820,13 +916,22 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
 
 }  // namespace
 
-cudaError_t tf32x3_init(int* pair_clusters) {
-  cudaError_t e = cudaFuncSetAttribute(
-      k_tf32x3, cudaFuncAttributeMaxDynamicSharedMemorySize, int(X_SMEM));
+template <int OA, int OB>
+cudaError_t set_smem_attrs() {
+  const cudaError_t e = cudaFuncSetAttribute(
+      k_tf32x3<OA, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      int(X_SMEM));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_tf32x3_pair,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(P_SMEM));
+  return cudaFuncSetAttribute(k_tf32x3_pair<OA, OB>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(P_SMEM));
+}
+
+cudaError_t tf32x3_init(int* pair_clusters) {
+  cudaError_t e = set_smem_attrs<0, 0>();
+  if (e == cudaSuccess) e = set_smem_attrs<0, 1>();
+  if (e == cudaSuccess) e = set_smem_attrs<1, 0>();
+  if (e == cudaSuccess) e = set_smem_attrs<1, 1>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
@@ -840,7 +945,7 @@ cudaError_t tf32x3_init(int* pair_clusters) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, k_tf32x3_pair, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, k_tf32x3_pair<0, 0>, &cfg);
   if (e != cudaSuccess) return e;
   *pair_clusters = n;
   return n > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
@@ -910,6 +1015,7 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   p.counters = counters;
   p.vec_store = (g.ldc % 4 == 0) &&
                 (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
+  p.sc = g.sc;
   p.status = status;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2u * unsigned(pl.G), 1, 1);
@@ -923,7 +1029,12 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_tf32x3_pair, tmA, tmB, p);
+  switch (g.op_a * 2 + g.op_b) {
+    case 0: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0>, tmA, tmB, p);
+    case 1: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1>, tmA, tmB, p);
+    case 2: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0>, tmA, tmB, p);
+    default: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1>, tmA, tmB, p);
+  }
 }
 
 cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
@@ -933,9 +1044,18 @@ cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
   const int tiles_n = int((g.N + XN - 1) / XN);
   const bool vec = (g.ldc % 4 == 0) &&
                    (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
-  k_tf32x3<<<unsigned(tiles_m) * unsigned(tiles_n), X_THREADS, X_SMEM, s>>>(
-      tmA, tmB, g.C, int(g.M), int(g.N), int(g.K), (long long)g.ldc, tiles_m,
-      tiles_n, vec ? 1 : 0, status);
+  const unsigned grid = unsigned(tiles_m) * unsigned(tiles_n);
+  auto go = [&](auto kernel) {
+    kernel<<<grid, X_THREADS, X_SMEM, s>>>(
+        tmA, tmB, g.C, int(g.M), int(g.N), int(g.K), (long long)g.ldc,
+        tiles_m, tiles_n, vec ? 1 : 0, g.sc, status);
+  };
+  switch (g.op_a * 2 + g.op_b) {
+    case 0: go(k_tf32x3<0, 0>); break;
+    case 1: go(k_tf32x3<0, 1>); break;
+    case 2: go(k_tf32x3<1, 0>); break;
+    default: go(k_tf32x3<1, 1>); break;
+  }
   return cudaGetLastError();
 }
 

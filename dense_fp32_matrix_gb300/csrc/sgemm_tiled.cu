@@ -130,7 +130,8 @@ __device__ __forceinline__ void zero_acc(f2 (&acc)[TM][TJ]) {
 // h covers columns n0 + c0 + COL_SPLIT h + {0..3}.
 __device__ __forceinline__ void store_tile(const f2 (&acc)[TM][TJ], float* C,
                                            int M, int N, long long ldc, int m0,
-                                           int n0, int r0, int c0, bool vec) {
+                                           int n0, int r0, int c0, bool vec,
+                                           const Scale& sc) {
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
     const int r = m0 + r0 + LANES_M * i;
@@ -140,17 +141,17 @@ __device__ __forceinline__ void store_tile(const f2 (&acc)[TM][TJ], float* C,
     for (int h = 0; h < TNC; ++h) {
       const int c = n0 + c0 + COL_SPLIT * h;
       if (vec && c + 3 < N) {
-        ulonglong2 v;
-        v.x = acc[i][2 * h].v;
-        v.y = acc[i][2 * h + 1].v;
-        *reinterpret_cast<ulonglong2*>(crow + c) = v;
+        float4 v;
+        f2_unpack(acc[i][2 * h], v.x, v.y);
+        f2_unpack(acc[i][2 * h + 1], v.z, v.w);
+        *reinterpret_cast<float4*>(crow + c) = epi4(v, crow + c, sc);
       } else {
         float x[4];
         f2_unpack(acc[i][2 * h], x[0], x[1]);
         f2_unpack(acc[i][2 * h + 1], x[2], x[3]);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (c + e < N) crow[c + e] = x[e];
+          if (c + e < N) crow[c + e] = epi1(x[e], crow + c + e, sc);
       }
     }
   }
@@ -195,6 +196,7 @@ struct SkParams {
   float* ws;               // 2 G partial tiles of BM x BN floats
   int* counters;           // one per tile, zero between calls
   int vec_store;
+  Scale sc;
   int* status;
 };
 
@@ -263,7 +265,7 @@ __device__ __forceinline__ void sk_fixup(const f2 (&acc)[TM][TJ], int tile,
     const int slot = 2 * cj + (range_begin(cj, p) >= x0 ? 0 : 1);
     add_partial(sum, ws + (long long)slot * SLOT);
   }
-  store_tile(sum, C, p.M, p.N, p.ldc, m0, n0, r0, c0, p.vec_store != 0);
+  store_tile(sum, C, p.M, p.N, p.ldc, m0, n0, r0, c0, p.vec_store != 0, p.sc);
   if (threadIdx.x == 0) p.counters[tile] = 0;
 }
 
@@ -368,7 +370,7 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
       tile_coords(tile, p.tiles_m, p.tiles_n, pm, pn);
       if (it_begin <= tile_begin && it + 1 == tile_end)
         store_tile(acc, C, p.M, p.N, p.ldc, pm * BM, pn * BN, lane_row0(tid),
-                   lane_col0(tid), p.vec_store != 0);
+                   lane_col0(tid), p.vec_store != 0, p.sc);
       else
         sk_fixup(acc, tile, 2 * blockIdx.x + (it_begin >= tile_begin ? 0 : 1),
                  p, C, pm * BM, pn * BN, lane_row0(tid), lane_col0(tid),
@@ -387,7 +389,7 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
 __global__ void __launch_bounds__(NT, MIN_BLOCKS)
 k_tiled_ldg(const float* __restrict__ A, long long lda,
             const float* __restrict__ B, long long ldb, float* __restrict__ C,
-            int M, int N, int K, long long ldc, int vec_store) {
+            int M, int N, int K, long long ldc, int vec_store, Scale sc) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
   uint8_t* sA = smem;
@@ -459,7 +461,7 @@ k_tiled_ldg(const float* __restrict__ A, long long lda,
   }
   cp_async_wait<0>();
   store_tile(acc, C, M, N, ldc, m0, n0, lane_row0(tid), lane_col0(tid),
-             vec_store != 0);
+             vec_store != 0, sc);
 }
 
 int grid_tiles(const GemmArgs& g) {
@@ -516,6 +518,7 @@ cudaError_t launch_tiled_tma(const GemmArgs& g, const CUtensorMap& tmA,
   p.ws = ws;
   p.counters = counters;
   p.vec_store = vec_ok(g) ? 1 : 0;
+  p.sc = g.sc;
   p.status = status;
   k_tiled_tma<<<pl.grid, NT, SMEM_BYTES, s>>>(tmA, tmB, g.C, p);
   return cudaGetLastError();
@@ -525,7 +528,7 @@ cudaError_t launch_tiled_ldg(const GemmArgs& g, int* status, cudaStream_t s) {
   (void)status;
   k_tiled_ldg<<<grid_tiles(g), NT, SMEM_BYTES, s>>>(
       g.A, (long long)g.lda, g.B, (long long)g.ldb, g.C, int(g.M), int(g.N),
-      int(g.K), (long long)g.ldc, vec_ok(g) ? 1 : 0);
+      int(g.K), (long long)g.ldc, vec_ok(g) ? 1 : 0, g.sc);
   return cudaGetLastError();
 }
 

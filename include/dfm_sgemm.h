@@ -82,6 +82,10 @@ extern "C" {
 #define SGEMM_MATH_AUTO 0  /* fastest path within the accuracy contract     */
 #define SGEMM_MATH_FFMA 1  /* CUDA-core fp32 fused multiply-add paths only   */
 
+/* Operand forms (sgemm_ex): op(X) = X or its transpose. */
+#define SGEMM_OP_N 0  /* as stored, row-major                               */
+#define SGEMM_OP_T 1  /* transposed: the stored rows are op(X)'s columns    */
+
 /* Kernel paths (sgemm_path / sgemm_plan). */
 #define SGEMM_PATH_AUTO 0
 #define SGEMM_PATH_TILED_TMA 1  /* TMA-fed multistage tile kernel (aligned) */
@@ -115,6 +119,46 @@ int sgemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
 int sgemm_path(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                const float* B, int64_t ldb, float* C, int64_t ldc,
                void* stream, int path);
+
+/*
+ * sgemm_ex: C = alpha * op(A) * op(B) + beta * C, on `stream`.
+ *   op(A) is M x K: op_a == SGEMM_OP_N, A stored M x K (row i at A + i*lda,
+ *   lda >= max(1, K)); SGEMM_OP_T, A stored K x M (op(A)_ik = A[k*lda + i],
+ *   lda >= max(1, M)).
+ *   op(B) is K x N: op_b == SGEMM_OP_N, B stored K x N (ldb >= max(1, N));
+ *   SGEMM_OP_T, B stored N x K (op(B)_kj = B[j*ldb + k], ldb >= max(1, K)).
+ *   C is M x N (ldc >= max(1, N)); its pitch padding is never touched.
+ * BLAS conventions: with beta == 0, C is not read (it may hold NaN); with
+ * alpha == 0 or K == 0, A and B are not read (may be NULL) and C = beta * C
+ * (C untouched when beta == 1). sgemm(...) is sgemm_ex(SGEMM_OP_N,
+ * SGEMM_OP_N, ..., alpha = 1, ..., beta = 0, ...), with identical results.
+ * The pages compute only the plain product; the operand forms and scalars
+ * are the BLAS reading of the cuBLAS call they discuss ("GEMM from naive to
+ * tiled", sections 二.2, 九.2). Accuracy: every element satisfies
+ *   |C - C_exact| <= 1e-4 * (|alpha| * sum_k |op(A)_ik op(B)_kj|
+ *                            + |beta * C_old|) + 1e-6.
+ * The tensor-core kernels read transposed operands in place; the CUDA-core
+ * kernels get row-major copies made in the stream's workspace (a
+ * bandwidth-bound transpose, grown like the stream-K workspace).
+ * Errors: as sgemm, plus SGEMM_ERR_INVALID_VALUE for an unknown op.
+ */
+int sgemm_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+             float alpha, const float* A, int64_t lda, const float* B,
+             int64_t ldb, float beta, float* C, int64_t ldc, void* stream);
+
+/* sgemm_ex_path: sgemm_ex on a forced kernel path (as sgemm_path). */
+int sgemm_ex_path(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                  float alpha, const float* A, int64_t lda, const float* B,
+                  int64_t ldb, float beta, float* C, int64_t ldc, void* stream,
+                  int path);
+
+/*
+ * sgemm_plan_ex: the kernel path sgemm_ex would take (for alpha != 0),
+ * decided on the host only; as sgemm_plan.
+ */
+int sgemm_plan_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc, uint64_t a_addr,
+                  uint64_t b_addr, uint64_t c_addr, int* path);
 
 /*
  * sgemm_set_math_mode: SGEMM_MATH_AUTO (default) or SGEMM_MATH_FFMA, for the

@@ -121,7 +121,7 @@ def gemm_ex(op_a, op_b, alpha, A, B, beta, C0, M, N, K, lda=None, ldb=None,
         if X is None:
             return None, max(cols, 1)
         X = np.ascontiguousarray(X, dtype=np.float32)
-        return X, (X.shape[1] if X.ndim == 2 else max(cols, 1))
+        return X, max(X.shape[1] if X.ndim == 2 else cols, 1)
     A, lda_d = prep(A, M if oa else K)
     B, ldb_d = prep(B, K if ob else N)
     C0, ldc_d = prep(C0, N)
