@@ -13,7 +13,7 @@ from . import _native
 
 __all__ = [
     "SgemmError", "sgemm", "sgemm_path", "sgemm_plan", "sgemm_host",
-    "sgemm_ex", "sgemm_plan_ex", "OPS",
+    "sgemm_ex", "sgemm_plan_ex", "sgemm_strided_batched", "OPS",
     "sgemm_noalloc", "sgemm_set_math_mode", "MATH",
     "sgemm_watchdog_status", "sgemm_watchdog_selftest",
     "sgemm_status_string", "sgemm_path_name", "sgemm_version", "matmul",
@@ -115,6 +115,22 @@ def sgemm_plan_ex(op_a, op_b, M, N, K, lda, ldb, ldc, a_addr, b_addr,
                                        ldb, ldc, a_addr, b_addr, c_addr,
                                        ctypes.byref(out)), "sgemm_plan_ex")
     return sgemm_path_name(out.value)
+
+
+def sgemm_strided_batched(op_a, op_b, M, N, K, alpha, A, lda, stride_a, B,
+                          ldb, stride_b, beta, C, ldc, stride_c, batch,
+                          stream=None, path="auto") -> None:
+    """``batch`` products C_b = alpha op(A_b) op(B_b) + beta C_b with X_b =
+    X + b * stride_x (floats; stride 0 shares the operand) on ``stream``."""
+    lib = _native.lib()
+    args = (_op(op_a), _op(op_b), M, N, K, float(alpha), _ptr(A), lda,
+            stride_a, _ptr(B), ldb, stride_b, float(beta), _ptr(C), ldc,
+            stride_c, batch, _stream(stream))
+    if path == "auto":
+        rc = lib.sgemm_strided_batched(*args)
+    else:
+        rc = lib.sgemm_strided_batched_path(*args, _path(path))
+    _check(rc, "sgemm_strided_batched")
 
 
 def sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> None:

@@ -36,6 +36,14 @@ _SIGNATURES = {
     "sgemm_plan_ex": ([_int, _int, _i64, _i64, _i64, _i64, _i64, _i64,
                        ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
                        ctypes.POINTER(_int)], _int),
+    "sgemm_strided_batched": ([_int, _int, _i64, _i64, _i64, ctypes.c_float,
+                               _vp, _i64, _i64, _vp, _i64, _i64,
+                               ctypes.c_float, _vp, _i64, _i64, _i64, _vp],
+                              _int),
+    "sgemm_strided_batched_path": ([_int, _int, _i64, _i64, _i64,
+                                    ctypes.c_float, _vp, _i64, _i64, _vp,
+                                    _i64, _i64, ctypes.c_float, _vp, _i64,
+                                    _i64, _i64, _vp, _int], _int),
     "sgemm_noalloc": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp],
                       _int),
     "sgemm_host": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp,

@@ -49,6 +49,11 @@ struct GemmArgs {
   Scale sc = Scale();
   int op_a = 0;
   int op_b = 0;
+  // Strided batch (tensor-core kernels only): item b reads A + b * stride_a
+  // and B + b * stride_b (stride 0: one operand shared by every item) and
+  // writes C + b * stride_c.
+  int64_t batch = 1;
+  int64_t stride_a = 0, stride_b = 0, stride_c = 0;
 };
 
 // Tile geometry of the main kernel (also used by the host dispatcher).
@@ -141,7 +146,7 @@ struct PairPlan {
 // fix-up; the schedule widens the split part by a wave instead.
 constexpr int kPairMinSkIters = 8;
 PairPlan plan_pair(int64_t M, int64_t N, int64_t K, int clusters,
-                   bool stream_k);
+                   bool stream_k, int64_t batch = 1);
 cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
                                const CUtensorMap& tmB, const PairPlan& pl,
                                float* ws, int* counters, int* status,

@@ -246,6 +246,32 @@ int encode_2d(CUtensorMap* map, const float* base, int64_t inner,
              : SGEMM_ERR_CUDA;
 }
 
+// 3-D fp32 map {inner, outer, items}: rows ld floats apart, items `stride`
+// floats apart (one item: stride = the packed ld * outer), box
+// {box_inner, box_outer, 1}.
+int encode_3d(CUtensorMap* map, const float* base, int64_t inner,
+              int64_t outer, int64_t ld, int64_t items, int64_t stride,
+              uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return SGEMM_ERR_CUDA;
+  if (items <= 1) {
+    items = 1;
+    stride = ld * outer;
+  }
+  const cuuint64_t dims[3] = {cuuint64_t(inner), cuuint64_t(outer),
+                              cuuint64_t(items)};
+  const cuuint64_t strides[2] = {cuuint64_t(ld) * 4, cuuint64_t(stride) * 4};
+  const cuuint32_t box[3] = {box_inner, box_outer, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? SGEMM_OK
+             : SGEMM_ERR_CUDA;
+}
+
 int encode_1d(CUtensorMap* map, const float* base, int64_t n, uint32_t box) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return SGEMM_ERR_CUDA;
@@ -308,18 +334,21 @@ int to_status(cudaError_t e) {
 // stored N x K) is one box {32 k, 128 rows}; an MN-major one (A stored
 // K x M, or B stored K x N) is read as boxes {32 rows, 32 k}. All with the
 // 128-byte swizzle.
+// The third dimension is the batch item (extent 1 unless the operand
+// differs between items).
 int encode_tf32x3(const GemmArgs& g, CUtensorMap* tmA, CUtensorMap* tmB) {
+  const int64_t ia = g.batch > 1 && g.stride_a != 0 ? g.batch : 1;
+  const int64_t ib = g.batch > 1 && g.stride_b != 0 ? g.batch : 1;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const int rc =
       g.op_a == 0
-          ? encode_2d(tmA, g.A, g.K, g.M, g.lda, 32, 128,
-                      CU_TENSOR_MAP_SWIZZLE_128B)
-          : encode_2d(tmA, g.A, g.M, g.K, g.lda, 32, 32,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+          ? encode_3d(tmA, g.A, g.K, g.M, g.lda, ia, g.stride_a, 32, 128, sw)
+          : encode_3d(tmA, g.A, g.M, g.K, g.lda, ia, g.stride_a, 32, 32, sw);
   if (rc != SGEMM_OK) return rc;
-  return g.op_b == 0 ? encode_2d(tmB, g.B, g.N, g.K, g.ldb, 32, 32,
-                                 CU_TENSOR_MAP_SWIZZLE_128B)
-                     : encode_2d(tmB, g.B, g.K, g.N, g.ldb, 32, 128,
-                                 CU_TENSOR_MAP_SWIZZLE_128B);
+  return g.op_b == 0
+             ? encode_3d(tmB, g.B, g.N, g.K, g.ldb, ib, g.stride_b, 32, 32, sw)
+             : encode_3d(tmB, g.B, g.K, g.N, g.ldb, ib, g.stride_b, 32, 128,
+                         sw);
 }
 
 // (st.ws_mu held: the pair kernel uses the stream's workspace.)
@@ -329,7 +358,8 @@ int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
   const int rc = encode_tf32x3(g, &tmA, &tmB);
   if (rc != SGEMM_OK) return rc;
   if (!pair) return to_status(launch_tf32x3(g, tmA, tmB, st.status, s));
-  const PairPlan pl = plan_pair(g.M, g.N, g.K, st.pair_clusters, true);
+  const PairPlan pl =
+      plan_pair(g.M, g.N, g.K, st.pair_clusters, true, g.batch);
   Workspace* w = nullptr;
   const int wrc = ensure_workspace(st, s, pl.ws_floats, pl.counters, &w);
   if (wrc != SGEMM_OK) return wrc;
@@ -560,6 +590,90 @@ int run(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   return run_call(c, stream, path);
 }
 
+// ---------------------------------------------------------------- batches
+//
+// Item b: C_b = alpha * op(A_b) * op(B_b) + beta * C_b with X_b = X + b *
+// stride_x (stride 0: one operand shared by every item). The tensor-core
+// kernels take the whole batch in one launch (3-D tensor maps, tiles of all
+// items in one persistent schedule); every other path runs item by item.
+int run_batched(const Call& c, int64_t stride_a, int64_t stride_b,
+                int64_t stride_c, int64_t batch, void* stream, int path) {
+  int rc = check_call(c);
+  if (rc != SGEMM_OK) return rc;
+  if (path < 0 || path >= SGEMM_PATH_COUNT) return SGEMM_ERR_INVALID_VALUE;
+  if (batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0)
+    return SGEMM_ERR_INVALID_VALUE;
+  if (batch == 0 || c.M == 0 || c.N == 0) return SGEMM_OK;
+  if (batch == 1) return run_call(c, stream, path);
+  // Items of C must not share memory: stacked (each item past the previous
+  // one's last element) or side by side inside one row pitch.
+  const bool stacked = stride_c >= (c.M - 1) * c.ldc + c.N;
+  const bool side_by_side =
+      stride_c >= c.N && (batch - 1) * stride_c + c.N <= c.ldc;
+  if (!stacked && !side_by_side) return SGEMM_ERR_INVALID_VALUE;
+  if (batch > kMaxDim) return SGEMM_ERR_TOO_LARGE;
+  if (reads_ab(c)) {  // C (all items) against A and B (all items)
+    const uint64_t cc = reinterpret_cast<uint64_t>(c.C);
+    const uint64_t c_hi =
+        cc + uint64_t(((batch - 1) * stride_c + (c.M - 1) * c.ldc + c.N) * 4);
+    auto hits = [&](const float* x, int64_t rows, int64_t cols, int64_t ld,
+                    int64_t stride) {
+      const uint64_t lo = reinterpret_cast<uint64_t>(x);
+      const uint64_t hi =
+          lo + uint64_t(((batch - 1) * stride + (rows - 1) * ld + cols) * 4);
+      return lo < c_hi && cc < hi;
+    };
+    if (hits(c.A, c.op_a ? c.K : c.M, c.op_a ? c.M : c.K, c.lda, stride_a) ||
+        hits(c.B, c.op_b ? c.N : c.K, c.op_b ? c.K : c.N, c.ldb, stride_b))
+      return SGEMM_ERR_OVERLAP;
+  }
+  const bool strides_ok = stride_a % 4 == 0 && stride_b % 4 == 0;
+  const int64_t pair_tiles = ((c.M + 255) / 256) * ((c.N + 255) / 256);
+  const int64_t tiles = ((c.M + kTileM - 1) / kTileM) *
+                        ((c.N + kTileN - 1) / kTileN);
+  const bool tensor_ok =
+      reads_ab(c) && strides_ok &&
+      tma_operand_ok(reinterpret_cast<uint64_t>(c.A), c.lda) &&
+      tma_operand_ok(reinterpret_cast<uint64_t>(c.B), c.ldb) &&
+      batch * tiles < (int64_t(1) << 31);
+  if (path == SGEMM_PATH_AUTO && tensor_ok &&
+      g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO &&
+      c.M > 1 && c.N > 1)
+    path = batch * pair_tiles >= kTf32PairMinTiles ? SGEMM_PATH_TF32X3_PAIR
+                                                   : SGEMM_PATH_TF32X3;
+  if (reads_ab(c) &&
+      (path == SGEMM_PATH_TF32X3 || path == SGEMM_PATH_TF32X3_PAIR)) {
+    if (!tensor_ok) return SGEMM_ERR_PATH;
+    DeviceState* st = nullptr;
+    rc = device_state(&st);
+    if (rc != SGEMM_OK) return rc;
+    GemmArgs g{c.M, c.N, c.K, c.A, c.lda, c.B, c.ldb, c.C, c.ldc};
+    g.sc.alpha = c.alpha;
+    g.sc.beta = c.beta;
+    g.op_a = c.op_a;
+    g.op_b = c.op_b;
+    g.batch = batch;
+    g.stride_a = stride_a;
+    g.stride_b = stride_b;
+    g.stride_c = stride_c;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(st->ws_mu);
+    rc = run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR);
+    // a batch layout the tensor-map encoder refuses runs item by item
+    if (rc != SGEMM_ERR_CUDA) return rc;
+    path = SGEMM_PATH_AUTO;
+  }
+  for (int64_t b = 0; b < batch; ++b) {
+    Call item = c;
+    item.A = c.A + b * stride_a;
+    item.B = c.B + b * stride_b;
+    item.C = c.C + b * stride_c;
+    rc = run_call(item, stream, path);
+    if (rc != SGEMM_OK) return rc;
+  }
+  return SGEMM_OK;
+}
+
 }  // namespace
 
 int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
@@ -787,6 +901,27 @@ int sgemm_plan_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
   if (rc != SGEMM_OK) return rc;
   *path = dfm::plan_call(c);
   return SGEMM_OK;
+}
+
+int sgemm_strided_batched(int op_a, int op_b, int64_t M, int64_t N,
+                          int64_t K, float alpha, const float* A, int64_t lda,
+                          int64_t stride_a, const float* B, int64_t ldb,
+                          int64_t stride_b, float beta, float* C, int64_t ldc,
+                          int64_t stride_c, int64_t batch, void* stream) {
+  const dfm::Call c{op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc};
+  return dfm::run_batched(c, stride_a, stride_b, stride_c, batch, stream,
+                          SGEMM_PATH_AUTO);
+}
+
+int sgemm_strided_batched_path(int op_a, int op_b, int64_t M, int64_t N,
+                               int64_t K, float alpha, const float* A,
+                               int64_t lda, int64_t stride_a, const float* B,
+                               int64_t ldb, int64_t stride_b, float beta,
+                               float* C, int64_t ldc, int64_t stride_c,
+                               int64_t batch, void* stream, int path) {
+  const dfm::Call c{op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc};
+  return dfm::run_batched(c, stride_a, stride_b, stride_c, batch, stream,
+                          path);
 }
 
 int sgemm_set_math_mode(int mode) {

@@ -182,42 +182,58 @@ __device__ __forceinline__ void split_transpose_half(uint8_t* box,
 //     four boxes {32 rows, 32 k} land N-major and are transposed in place
 //     into K-major rows (split_transpose_box / _half).
 // (128-row halves: the 1-SM kernel's tile and each block's half of a pair.)
+// The maps are 3-D: {inner, outer, batch item}; za / zb pick the item of
+// A / B (0 for an operand shared by all items).
 template <int OA, int OB>
 __device__ __forceinline__ void load_stage(uint8_t* a_buf, uint8_t* b_buf,
                                            const CUtensorMap* tmA,
                                            const CUtensorMap* tmB, int k,
-                                           int m0, int n0, uint32_t bar) {
+                                           int m0, int n0, int za, int zb,
+                                           uint32_t bar) {
   if (OA == 0) {
-    tma_load_2d(smem_u32(a_buf), tmA, k * XK, m0, bar);
+    tma_load_3d(smem_u32(a_buf), tmA, k * XK, m0, za, bar);
   } else {
     for (int j = 0; j < 4; ++j)
-      tma_load_2d(smem_u32(a_buf + j * X_B_BOX), tmA, m0 + 32 * j, k * XK,
+      tma_load_3d(smem_u32(a_buf + j * X_B_BOX), tmA, m0 + 32 * j, k * XK, za,
                   bar);
   }
   if (OB == 0) {
     for (int j = 0; j < 4; ++j)
-      tma_load_2d(smem_u32(b_buf + j * X_B_BOX), tmB, n0 + 32 * j, k * XK,
+      tma_load_3d(smem_u32(b_buf + j * X_B_BOX), tmB, n0 + 32 * j, k * XK, zb,
                   bar);
   } else {
-    tma_load_2d(smem_u32(b_buf), tmB, k * XK, n0, bar);
+    tma_load_3d(smem_u32(b_buf), tmB, k * XK, n0, zb, bar);
   }
 }
 
 template <int OA, int OB>
 __device__ __forceinline__ void prefetch_stage(const CUtensorMap* tmA,
                                                const CUtensorMap* tmB, int k,
-                                               int m0, int n0) {
+                                               int m0, int n0, int za,
+                                               int zb) {
   if (OA == 0) {
-    tma_prefetch_l2_2d(tmA, k * XK, m0);
+    tma_prefetch_l2_3d(tmA, k * XK, m0, za);
   } else {
-    for (int j = 0; j < 4; ++j) tma_prefetch_l2_2d(tmA, m0 + 32 * j, k * XK);
+    for (int j = 0; j < 4; ++j)
+      tma_prefetch_l2_3d(tmA, m0 + 32 * j, k * XK, za);
   }
   if (OB == 0) {
-    for (int j = 0; j < 4; ++j) tma_prefetch_l2_2d(tmB, n0 + 32 * j, k * XK);
+    for (int j = 0; j < 4; ++j)
+      tma_prefetch_l2_3d(tmB, n0 + 32 * j, k * XK, zb);
   } else {
-    tma_prefetch_l2_2d(tmB, k * XK, n0);
+    tma_prefetch_l2_3d(tmB, k * XK, n0, zb);
   }
 }
+
+// Batch description shared by the tensor-core kernels: tiles are numbered
+// item by item (tiles_m x tiles_n per item, grouped raster order inside an
+// item); C of item b starts at C + b * stride_c.
+struct Batch {
+  int items;            // >= 1
+  int a_batched;        // 0: every item reads item 0 of A (shared A)
+  int b_batched;
+  long long stride_c;   // floats
+};
 
 // 1-SM kernel: 4 split warps (w = 0..3, ct = 0..127). K-major operands are
 // split elementwise by all of them (hi masked in place, lo beside), an
@@ -258,7 +274,7 @@ __global__ void __launch_bounds__(X_THREADS, 1)
 k_tf32x3(const __grid_constant__ CUtensorMap tmA,
          const __grid_constant__ CUtensorMap tmB, float* __restrict__ C, int M,
          int N, int K, long long ldc, int tiles_m, int tiles_n, int vec_store,
-         Scale sc, int* status) {
+         Scale sc, Batch bt, int* status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -278,8 +294,12 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int pm, pn;
-  tile_of(blockIdx.x, tiles_m, tiles_n, pm, pn);
+  const int tpb = tiles_m * tiles_n;
+  const int item = int(blockIdx.x) / tpb;
+  tile_of(int(blockIdx.x) - item * tpb, tiles_m, tiles_n, pm, pn);
   const int m0 = pm * XM, n0 = pn * XN;
+  const int za = bt.a_batched ? item : 0, zb = bt.b_batched ? item : 0;
+  C += item * bt.stride_c;
   const int T = (K + XK - 1) / XK;
 
   if (tid == 0) {
@@ -316,7 +336,8 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
         }
         const uint32_t bar = full0 + 8 * s;
         mbar_arrive_expect_tx(bar, X_A_BYTES + X_B_BYTES);
-        load_stage<OA, OB>(A_of(s), B_of(s), &tmA, &tmB, t, m0, n0, bar);
+        load_stage<OA, OB>(A_of(s), B_of(s), &tmA, &tmB, t, m0, n0, za, zb,
+                           bar);
       }
     }
   } else if (warp == 1) {
@@ -471,8 +492,17 @@ struct PairParams {
   int* counters;        // sk_tiles x 2 blocks x 4 quarters, zero between calls
   int vec_store;
   Scale sc;
+  Batch bt;
   int* status;
 };
+
+// Tile t of the pair schedule -> batch item and 256 x 256 tile in it.
+__device__ __forceinline__ void pair_tile(int t, const PairParams& p, int& item,
+                                          int& pm, int& pn) {
+  const int tpb = p.tiles_m * p.tiles_n;
+  item = t / tpb;
+  tile_of(t - item * tpb, p.tiles_m, p.tiles_n, pm, pn);
+}
 
 // Pair kernel: 8 split warps (cw = 0..7, ct = 0..255). K-major operands:
 // the landed tile is the high part, all threads write the low part. One
@@ -662,10 +692,12 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       int g = 0;  // stages issued
       Unit w;
       for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
-        int pm, pn;
-        tile_of(w.tile, p.tiles_m, p.tiles_n, pm, pn);
+        int item, pm, pn;
+        pair_tile(w.tile, p, item, pm, pn);
         const int m_own = pm * PM + 128 * int(rank);
         const int n_own = pn * PN + 128 * int(rank);
+        const int za = p.bt.a_batched ? item : 0;
+        const int zb = p.bt.b_batched ? item : 0;
         for (int k = w.kb; k < w.ke; ++k, ++g) {
           const int s = g % XSTAGES;
           if (g >= XSTAGES &&
@@ -676,12 +708,13 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
           }
           const uint32_t bar = full0 + 8 * s;
           mbar_arrive_expect_tx(bar, X_A_BYTES + X_B_BYTES);
-          load_stage<OA, OB>(A_of(s), B_of(s), &tmA, &tmB, k, m_own, n_own,
-                             bar);
+          load_stage<OA, OB>(A_of(s), B_of(s), &tmA, &tmB, k, m_own, n_own, za,
+                             zb, bar);
           // warm L2 with the tiles of a later k-slice of this unit, so that
           // its load (issued when a stage frees up) is an L2 hit
           if (k + P_PREFETCH < w.ke)
-            prefetch_stage<OA, OB>(&tmA, &tmB, k + P_PREFETCH, m_own, n_own);
+            prefetch_stage<OA, OB>(&tmA, &tmB, k + P_PREFETCH, m_own, n_own,
+                                   za, zb);
         }
       }
       // Let the last loads land before the block can exit (they complete
@@ -815,11 +848,11 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       tc::fence_after_sync();
       const uint32_t acc = tmem + uint32_t(b * P_ACC_COLS) +
                            (uint32_t(32 * quarter) << 16);
-      int pm, pn;
-      tile_of(w.tile, p.tiles_m, p.tiles_n, pm, pn);
+      int item, pm, pn;
+      pair_tile(w.tile, p, item, pm, pn);
       const int r = pm * PM + 128 * int(rank) + row;
       const int n0 = pn * PN;
-      float* crow = p.C + (long long)r * p.ldc;
+      float* crow = p.C + item * p.bt.stride_c + (long long)r * p.ldc;
       int slot = 0;
       if (w.sk < 0) {
         store_c_quarter(acc, crow, r < p.M, n0, p);
@@ -952,11 +985,11 @@ cudaError_t tf32x3_init(int* pair_clusters) {
 }
 
 PairPlan plan_pair(int64_t M, int64_t N, int64_t K, int clusters,
-                   bool stream_k) {
+                   bool stream_k, int64_t batch) {
   PairPlan pl;
   pl.tiles_m = int((M + PM - 1) / PM);
   pl.tiles_n = int((N + PN - 1) / PN);
-  pl.tiles = pl.tiles_m * pl.tiles_n;
+  pl.tiles = int(batch) * pl.tiles_m * pl.tiles_n;  // checked by the host
   pl.T = int((K + XK - 1) / XK);
   if (clusters < 1) clusters = 1;
   pl.G = pl.tiles < clusters ? pl.tiles : clusters;
@@ -1016,6 +1049,10 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   p.vec_store = (g.ldc % 4 == 0) &&
                 (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
   p.sc = g.sc;
+  p.bt.items = int(g.batch);
+  p.bt.a_batched = g.batch > 1 && g.stride_a != 0;
+  p.bt.b_batched = g.batch > 1 && g.stride_b != 0;
+  p.bt.stride_c = (long long)g.stride_c;
   p.status = status;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2u * unsigned(pl.G), 1, 1);
@@ -1044,11 +1081,17 @@ cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
   const int tiles_n = int((g.N + XN - 1) / XN);
   const bool vec = (g.ldc % 4 == 0) &&
                    (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
-  const unsigned grid = unsigned(tiles_m) * unsigned(tiles_n);
+  const unsigned grid = unsigned(g.batch) * unsigned(tiles_m) *
+                        unsigned(tiles_n);  // < 2^31, checked by the host
+  Batch bt;
+  bt.items = int(g.batch);
+  bt.a_batched = g.batch > 1 && g.stride_a != 0;
+  bt.b_batched = g.batch > 1 && g.stride_b != 0;
+  bt.stride_c = (long long)g.stride_c;
   auto go = [&](auto kernel) {
     kernel<<<grid, X_THREADS, X_SMEM, s>>>(
         tmA, tmB, g.C, int(g.M), int(g.N), int(g.K), (long long)g.ldc,
-        tiles_m, tiles_n, vec ? 1 : 0, g.sc, status);
+        tiles_m, tiles_n, vec ? 1 : 0, g.sc, bt, status);
   };
   switch (g.op_a * 2 + g.op_b) {
     case 0: go(k_tf32x3<0, 0>); break;

@@ -161,6 +161,39 @@ int sgemm_plan_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
                   uint64_t b_addr, uint64_t c_addr, int* path);
 
 /*
+ * sgemm_strided_batched: `batch` independent products
+ *   C_b = alpha * op(A_b) * op(B_b) + beta * C_b,   b = 0 .. batch - 1,
+ * with A_b = A + b * stride_a, B_b = B + b * stride_b, C_b = C + b * stride_c
+ * (strides in floats, >= 0; a stride of 0 shares that operand between all
+ * items, e.g. one weight matrix applied to a batch). Each item follows
+ * sgemm_ex (same forms, scalars, accuracy and unread-operand rules). The
+ * items of C must not share memory: either stacked, stride_c >= (M - 1) *
+ * ldc + N, or side by side in one row pitch, stride_c >= N and
+ * (batch - 1) * stride_c + N <= ldc; otherwise SGEMM_ERR_INVALID_VALUE.
+ * C must not overlap any item of A or B (SGEMM_ERR_OVERLAP). batch == 0 is
+ * a no-op. With 16-byte-aligned operands and strides that are multiples of
+ * 4 floats, the tensor-core kernels take the whole batch in one launch
+ * (one persistent schedule over the tiles of all items, so a shared
+ * operand is fetched from memory once for all of them: the batched product
+ * with a shared A that "如何让计算受限问题真正达到计算受限" (section 5.3,
+ * fusion) gives as an example of reading data once for several
+ * consumers); otherwise the items run one by one.
+ */
+int sgemm_strided_batched(int op_a, int op_b, int64_t M, int64_t N,
+                          int64_t K, float alpha, const float* A, int64_t lda,
+                          int64_t stride_a, const float* B, int64_t ldb,
+                          int64_t stride_b, float beta, float* C, int64_t ldc,
+                          int64_t stride_c, int64_t batch, void* stream);
+
+/* sgemm_strided_batched_path: as above on a forced kernel path. */
+int sgemm_strided_batched_path(int op_a, int op_b, int64_t M, int64_t N,
+                               int64_t K, float alpha, const float* A,
+                               int64_t lda, int64_t stride_a, const float* B,
+                               int64_t ldb, int64_t stride_b, float beta,
+                               float* C, int64_t ldc, int64_t stride_c,
+                               int64_t batch, void* stream, int path);
+
+/*
  * sgemm_set_math_mode: SGEMM_MATH_AUTO (default) or SGEMM_MATH_FFMA, for the
  * whole process, for calls that start after it returns. Returns the previous
  * mode, or SGEMM_ERR_INVALID_VALUE for an unknown mode.

@@ -29,6 +29,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("sgemm", "sgemm_path", "sgemm_plan", "sgemm_host",
               "sgemm_ex", "sgemm_ex_path", "sgemm_plan_ex",
+              "sgemm_strided_batched", "sgemm_strided_batched_path",
               "sgemm_set_math_mode",
               "sgemm_watchdog_status", "sgemm_watchdog_selftest",
               "sgemm_status_string", "sgemm_path_name", "sgemm_version"):
@@ -173,3 +174,19 @@ def test_ex_alpha_zero_reads_no_operand(lib):
                       None) == 0
     assert L.sgemm_ex(0, 0, 4, 4, 4, 1.0, None, 4, B16, 4, 0.0, C16, 4,
                       None) == -2
+
+
+def test_batched_argument_errors_before_any_device_work(lib):
+    L = _native.lib()
+    call = lambda sc, batch, sa=0, sb=0: L.sgemm_strided_batched(
+        0, 0, 8, 8, 8, 1.0, A16, 8, sa, B16, 8, sb, 0.0, C16, 8, sc, batch,
+        None)
+    assert call(64, 0) == 0                  # empty batch
+    assert call(63, 2) == -1                 # items of C overlap (stacked)
+    assert call(8, 2) == -1                  # side by side needs ldc >= 16
+    assert call(64, -1) == -1                # negative batch
+    assert call(64, 2, sa=-8) == -1          # negative stride
+    # side by side in one row pitch is fine: checked on the host, then the
+    # call would need a device (not reached here for an overlap error)
+    assert L.sgemm_strided_batched(0, 0, 8, 8, 8, 1.0, C16 + 4, 8, 0, B16, 8,
+                                   0, 0.0, C16, 16, 8, 2, None) == -6
