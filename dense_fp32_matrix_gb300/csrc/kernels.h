@@ -147,10 +147,12 @@ struct PairPlan {
 constexpr int kPairMinSkIters = 8;
 PairPlan plan_pair(int64_t M, int64_t N, int64_t K, int clusters,
                    bool stream_k, int64_t batch = 1);
+// tmC (may be null): C as dims {N, M, batch items}, box {32, 32, 1},
+// 128-byte swizzle; used for whole tiles when beta == 0.
 cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
-                               const CUtensorMap& tmB, const PairPlan& pl,
-                               float* ws, int* counters, int* status,
-                               cudaStream_t s);
+                               const CUtensorMap& tmB, const CUtensorMap* tmC,
+                               const PairPlan& pl, float* ws, int* counters,
+                               int* status, cudaStream_t s);
 
 // M == 1 and N == 1 bandwidth kernels for any layout; one-thread-per-output
 // kernel.

@@ -363,8 +363,16 @@ int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
   Workspace* w = nullptr;
   const int wrc = ensure_workspace(st, s, pl.ws_floats, pl.counters, &w);
   if (wrc != SGEMM_OK) return wrc;
-  return to_status(launch_tf32x3_pair(g, tmA, tmB, pl, w->ws, w->counters,
-                                      st.status, s));
+  // C by bulk tensor stores when it is not read (beta == 0) and aligned
+  CUtensorMap tmC;
+  const bool c_ok =
+      g.sc.beta == 0.f &&
+      tma_operand_ok(reinterpret_cast<uint64_t>(g.C), g.ldc) &&
+      (g.batch <= 1 || g.stride_c % 4 == 0) &&
+      encode_3d(&tmC, g.C, g.N, g.M, g.ldc, g.batch, g.stride_c, 32, 32,
+                CU_TENSOR_MAP_SWIZZLE_128B) == SGEMM_OK;
+  return to_status(launch_tf32x3_pair(g, tmA, tmB, c_ok ? &tmC : nullptr, pl,
+                                      w->ws, w->counters, st.status, s));
 }
 
 // ---------------------------------------------------------------- calls
@@ -731,8 +739,8 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
             cudaMemsetAsync(counters, 0, pl.counters * sizeof(int), s));
         if (rc != SGEMM_OK) return rc;
       }
-      return to_status(launch_tf32x3_pair(g, tmA, tmB, pl, ws, counters,
-                                          st->status, s));
+      return to_status(launch_tf32x3_pair(g, tmA, tmB, nullptr, pl, ws,
+                                          counters, st->status, s));
     }
     case SGEMM_PATH_GEMV_ROW: {
       const cudaError_t e = run_gemv_row(g, *st, s, &rc);

@@ -472,11 +472,19 @@ constexpr int P_PREFETCH = 3;                        // k-slices ahead into L2
 constexpr int P_CONV_WARPS = 8;
 constexpr int P_CONV_THREADS = 32 * P_CONV_WARPS;
 constexpr int P_ACC_COLS = 256;                      // one accumulator
-constexpr int P_TMEM_COLS = 2 * P_ACC_COLS;
+constexpr int P_TMEM_COLS = 2 * P_ACC_COLS;           // all of it
+constexpr int P_ALO_COL = P_ACC_COLS;                 // A_lo stages (K-major A)
+static_assert(P_ALO_COL + XSTAGES * XK <= P_TMEM_COLS, "A_lo stages fit");
 constexpr int P_EPI_WARP0 = 2 + P_CONV_WARPS;
 constexpr int P_EPI_ARRIVALS = 2 * 4;                // 4 warps x 2 blocks
 constexpr int P_PIECE_FLOATS = 128 * PN;             // one block's half tile
-constexpr size_t P_SMEM = size_t(XSTAGES) * X_STAGE + 1024 + 256;
+// Epilogue staging for the bulk tensor stores of C: per epilogue warp two
+// 4 KiB boxes of 32 rows x 32 columns (128-byte rows, 128-byte swizzle).
+constexpr int P_STG_BOX = 32 * 32 * 4;
+constexpr int P_STG_BYTES = 4 * 2 * P_STG_BOX;       // 32 KiB
+constexpr size_t P_SMEM =
+    size_t(XSTAGES) * X_STAGE + P_STG_BYTES + 1024 + 256;
+static_assert(P_SMEM <= 232448, "shared memory per block");
 
 struct PairParams {
   float* C;
@@ -491,6 +499,7 @@ struct PairParams {
   float* ws;            // 2 pieces per block: G x 2 x 2 x P_PIECE_FLOATS
   int* counters;        // sk_tiles x 2 blocks x 4 quarters, zero between calls
   int vec_store;
+  int tma_c;            // C written by bulk tensor stores (beta == 0)
   Scale sc;
   Batch bt;
   int* status;
@@ -504,6 +513,36 @@ __device__ __forceinline__ void pair_tile(int t, const PairParams& p, int& item,
   tile_of(t - item * tpb, p.tiles_m, p.tiles_n, pm, pn);
 }
 
+// Pair kernel, K-major A: A_lo goes to tensor memory instead of shared
+// memory (the MMA takes its A operand from there), which saves the split's
+// A_lo stores and the tensor core's A_lo reads in shared memory. Warp
+// 2 + cw may only reach tensor-memory lanes 32 q .. 32 q + 31 with
+// q = (2 + cw) & 3: it takes those rows of the block's 128 and the k half
+// cw >> 2. Each lane splits its row's 16 values from the 128-byte-swizzled
+// stage and stores the low parts to columns col + 16 (cw >> 2) .. + 15.
+__device__ __forceinline__ void a_lo_to_tmem(const uint8_t* A, uint32_t col,
+                                             int cw, int lane) {
+  const int q = (2 + cw) & 3, h = cw >> 2;
+  const int r = 32 * q + lane;
+  uint32_t lo[16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int chunk = 4 * h + c;
+    const float4 x = *reinterpret_cast<const float4*>(
+        A + r * 128 + ((chunk ^ (r & 7)) << 4));
+    float hi, l;
+    split_tf32(x.x, hi, l);
+    lo[4 * c + 0] = __float_as_uint(l);
+    split_tf32(x.y, hi, l);
+    lo[4 * c + 1] = __float_as_uint(l);
+    split_tf32(x.z, hi, l);
+    lo[4 * c + 2] = __float_as_uint(l);
+    split_tf32(x.w, hi, l);
+    lo[4 * c + 3] = __float_as_uint(l);
+  }
+  tc::tmem_st_32x32b_x16(col + (uint32_t(32 * q) << 16) + 16 * h, lo);
+}
+
 // Pair kernel: 8 split warps (cw = 0..7, ct = 0..255). K-major operands:
 // the landed tile is the high part, all threads write the low part. One
 // MN-major operand: two warps per box, one per 16-k half. Both MN-major:
@@ -511,14 +550,11 @@ __device__ __forceinline__ void pair_tile(int t, const PairParams& p, int& item,
 template <int OA, int OB>
 __device__ __forceinline__ void split_stage_pair(uint8_t* A, uint8_t* Alo,
                                                  uint8_t* B, uint8_t* Blo,
-                                                 int cw, int lane, int ct) {
+                                                 int cw, int lane, int ct,
+                                                 uint32_t alo_col) {
   constexpr int kThreads = 256;
   const int box = cw >> 1, half = cw & 1, bar_id = 1 + box;
-  if (OA == 0) {
-#pragma unroll
-    for (int q = 0; q < X_A_BYTES / 16 / kThreads; ++q)
-      split4_lo(A, Alo, ct + kThreads * q);
-  }
+  if (OA == 0) a_lo_to_tmem(A, alo_col, cw, lane);
   if (OB == 1) {
 #pragma unroll
     for (int q = 0; q < X_B_BYTES / 16 / kThreads; ++q)
@@ -631,14 +667,56 @@ __device__ __forceinline__ void store_c_quarter(uint32_t acc, float* crow,
   }
 }
 
+// One lane quarter's 32 rows x 256 columns of C from accumulator columns
+// `acc` through the warp's two staging boxes and bulk tensor stores (the
+// store clips rows >= M and columns >= N). Each lane writes its row of a
+// 32 x 32 box with the 128-byte swizzle (16-byte chunk c of row r at
+// c ^ (r & 7): conflict-free), then lane 0 stores the box. A box is reused
+// once the store issued from it two boxes earlier has read it.
+// One lane quarter's 32 rows x 256 columns of C from accumulator columns
+// `acc` through the warp's two staging boxes and bulk tensor stores (the
+// store clips rows >= M and columns >= N). Each lane writes its row of a
+// 32 x 32 box with the 128-byte swizzle (16-byte chunk c of row r at
+// c ^ (r & 7): conflict-free), then lane 0 stores the box. A box is reused
+// once the store issued from it two boxes earlier has read it.
+__device__ __forceinline__ void store_c_tma(uint32_t acc, uint8_t* stg,
+                                            const CUtensorMap* tmC, int lane,
+                                            int x0, int y0, int z,
+                                            float alpha) {
+#pragma unroll 1
+  for (int cb = 0; cb < PN / 32; ++cb) {
+    uint32_t v[32];
+    tc::tmem_ld_32x32b_x32(acc + 32 * cb, v);
+    tc::tmem_ld_wait();
+    uint8_t* box = stg + (cb & 1) * P_STG_BOX;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<float4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+          make_float4(alpha * __uint_as_float(v[4 * c]),
+                      alpha * __uint_as_float(v[4 * c + 1]),
+                      alpha * __uint_as_float(v[4 * c + 2]),
+                      alpha * __uint_as_float(v[4 * c + 3]));
+    fence_async_shared();  // generic writes -> visible to the bulk store
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tmC, smem_u32(box), x0 + 32 * cb, y0, z);
+      bulk_commit_group();
+    }
+  }
+}
+
 template <int OA, int OB>
 __global__ void __launch_bounds__(P_THREADS, 1)
 k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
-              const __grid_constant__ CUtensorMap tmB, const PairParams p) {
+              const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const PairParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t* ctrl = smem + XSTAGES * X_STAGE;
+  uint8_t* stg0 = smem + XSTAGES * X_STAGE;      // epilogue staging
+  uint8_t* ctrl = stg0 + P_STG_BYTES;
   const uint32_t full0 = smem_u32(ctrl);          // own TMA landed
   const uint32_t conv0 = full0 + 8 * XSTAGES;     // own split done
   const uint32_t empty0 = conv0 + 8 * XSTAGES;    // pair MMAs done reading
@@ -658,6 +736,11 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
   const int cl = int(blockIdx.x >> 1);
+  // K-major A: A_lo lives in tensor memory after the accumulator, so only
+  // one accumulator fits (the epilogue of a tile holds up the next tile's
+  // MMAs); otherwise two accumulators let them overlap.
+  constexpr bool kLoTmem = OA == 0;
+  constexpr int kAccs = kLoTmem ? 1 : 2;
 
   if (tid == 0) {
     for (int s = 0; s < XSTAGES; ++s) {
@@ -737,10 +820,10 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       int g = 0;
       Unit w;
       for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
-        const int b = u & 1;
-        if (u >= 2 &&
-            !mbar_wait_bounded<true>(acce0 + 8 * b, ((u >> 1) - 1) & 1,
-                                     p.status, kSiteTf32Acc, kWaitLimitNs)) {
+        const int b = u % kAccs, n = u / kAccs;
+        if (n >= 1 &&
+            !mbar_wait_bounded<true>(acce0 + 8 * b, (n - 1) & 1, p.status,
+                                     kSiteTf32Acc, kWaitLimitNs)) {
           *abort_flag = 1;
           break;
         }
@@ -770,8 +853,13 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
                                               tc::kLayoutSwizzle128);
             const uint64_t dbl = tc::smem_desc(bl + 32 * ks, 16, 1024,
                                                tc::kLayoutSwizzle128);
-            tc::mma_tf32_pair(acc, dal, db, idesc,
-                              (k > w.kb || ks > 0) ? 1u : 0u);
+            if (kLoTmem)
+              tc::mma_tf32_pair_tmem_a(
+                  acc, tmem + uint32_t(P_ALO_COL + XK * s + 8 * ks), db, idesc,
+                  (k > w.kb || ks > 0) ? 1u : 0u);
+            else
+              tc::mma_tf32_pair(acc, dal, db, idesc,
+                                (k > w.kb || ks > 0) ? 1u : 0u);
             tc::mma_tf32_pair(acc, da, dbl, idesc, 1u);
             tc::mma_tf32_pair(acc, da, db, idesc, 1u);
           }
@@ -799,6 +887,8 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
             *abort_flag = 1;
             break;
           }
+          tc::fence_after_sync();   // the split's tensor-memory stores ...
+          tc::fence_before_sync();  // ... ordered before the hand-over
           mbar_arrive_remote(peer_leader + 8 * s);
         }
       }
@@ -824,8 +914,16 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
           *abort_flag = 1;
           break;
         }
+        // the MMAs that read this stage's A_lo columns last time are done
+        // (their commit freed the stage before it was reloaded)
+        if (kLoTmem) tc::fence_after_sync();
         split_stage_pair<OA, OB>(A_of(s), Alo_of(s), B_of(s), Blo_of(s),
-                                 warp - 2, lane, ct);
+                                 warp - 2, lane, ct,
+                                 tmem + uint32_t(P_ALO_COL + XK * s));
+        if (kLoTmem) {
+          tc::tmem_st_wait();      // A_lo in tensor memory ...
+          tc::fence_before_sync();  // ... before the arrival
+        }
         fence_async_shared();  // generic writes -> visible to the MMA
         __syncwarp();
         if (lane == 0) mbar_arrive(conv0 + 8 * s);
@@ -839,8 +937,8 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
     float4* ws4 = reinterpret_cast<float4*>(p.ws);
     Unit w;
     for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
-      const int b = u & 1;
-      if (!mbar_wait_bounded(accf0 + 8 * b, (u >> 1) & 1, p.status,
+      const int b = u % kAccs;
+      if (!mbar_wait_bounded(accf0 + 8 * b, (u / kAccs) & 1, p.status,
                              kSiteTf32Acc, kWaitLimitNs)) {
         *abort_flag = 1;
         break;
@@ -854,7 +952,11 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       const int n0 = pn * PN;
       float* crow = p.C + item * p.bt.stride_c + (long long)r * p.ldc;
       int slot = 0;
-      if (w.sk < 0) {
+      if (w.sk < 0 && p.tma_c) {
+        store_c_tma(acc, stg0 + (warp - P_EPI_WARP0) * 2 * P_STG_BOX, &tmC,
+                    lane, n0, pm * PM + 128 * int(rank) + 32 * quarter, item,
+                    p.sc.alpha);
+      } else if (w.sk < 0) {
         store_c_quarter(acc, crow, r < p.M, n0, p);
       } else {
         // this block's piece: thread-major float4s, coalesced per warp
@@ -937,6 +1039,7 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       }
       if (lane == 0) *counter = 0;
     }
+    if (lane == 0) bulk_wait_group_all();  // C stores complete
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1028,9 +1131,9 @@ PairPlan plan_pair(int64_t M, int64_t N, int64_t K, int clusters,
 }
 
 cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
-                               const CUtensorMap& tmB, const PairPlan& pl,
-                               float* ws, int* counters, int* status,
-                               cudaStream_t s) {
+                               const CUtensorMap& tmB, const CUtensorMap* tmC,
+                               const PairPlan& pl, float* ws, int* counters,
+                               int* status, cudaStream_t s) {
   PairParams p;
   p.C = g.C;
   p.M = int(g.M);
@@ -1049,6 +1152,8 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   p.vec_store = (g.ldc % 4 == 0) &&
                 (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
   p.sc = g.sc;
+  p.tma_c = tmC != nullptr && g.sc.beta == 0.f;
+  const CUtensorMap& mapC = p.tma_c ? *tmC : tmA;  // unused without tma_c
   p.bt.items = int(g.batch);
   p.bt.a_batched = g.batch > 1 && g.stride_a != 0;
   p.bt.b_batched = g.batch > 1 && g.stride_b != 0;
@@ -1067,10 +1172,14 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   switch (g.op_a * 2 + g.op_b) {
-    case 0: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0>, tmA, tmB, p);
-    case 1: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1>, tmA, tmB, p);
-    case 2: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0>, tmA, tmB, p);
-    default: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1>, tmA, tmB, p);
+    case 0: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0>, tmA, tmB,
+                                     mapC, p);
+    case 1: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1>, tmA, tmB,
+                                     mapC, p);
+    case 2: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0>, tmA, tmB,
+                                     mapC, p);
+    default: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1>, tmA, tmB,
+                                     mapC, p);
   }
 }
 

@@ -140,6 +140,23 @@ __device__ __forceinline__ void commit_pair(uint32_t cluster_mbar) {
       : "memory");
 }
 
+// Pair MMA with A from tensor memory: A rows 0..127 in this CTA's lanes
+// 0..127 and rows 128..255 in the peer's, one 32-bit column per k (TF32),
+// at column a_tmem; B from shared memory as for mma_tf32_pair.
+__device__ __forceinline__ void mma_tf32_pair_tmem_a(uint32_t d_tmem,
+                                                    uint32_t a_tmem,
+                                                    uint64_t b_desc,
+                                                    uint32_t idesc,
+                                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on the mbarrier when all tcgen05 operations issued so far by
 // this thread have completed.
 __device__ __forceinline__ void commit(uint32_t mbar) {
@@ -168,6 +185,25 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr,
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
       : "r"(taddr));
+}
+
+// 32 lanes x 16 consecutive 32-bit columns from registers: thread t writes
+// lane (taddr.lane + t), columns taddr.col .. taddr.col + 15.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr,
+                                                   const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+      "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]),
+      "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Wait until this thread's tensor-memory stores have completed.
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
