@@ -712,38 +712,43 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
               const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const PairParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t* stg0 = smem + XSTAGES * X_STAGE;      // epilogue staging
-  uint8_t* ctrl = stg0 + P_STG_BYTES;
-  const uint32_t full0 = smem_u32(ctrl);          // own TMA landed
-  const uint32_t conv0 = full0 + 8 * XSTAGES;     // own split done
-  const uint32_t empty0 = conv0 + 8 * XSTAGES;    // pair MMAs done reading
-  const uint32_t peer0 = empty0 + 8 * XSTAGES;    // odd block split (even)
-  const uint32_t accf0 = peer0 + 8 * XSTAGES;     // accumulator b complete
-  const uint32_t acce0 = accf0 + 16;              // accumulator b read (even)
-  const uint32_t drain = acce0 + 16;              // teardown (even)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (4 * XSTAGES + 5));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  auto A_of = [&](int s) { return smem + s * X_STAGE; };
-  auto Alo_of = [&](int s) { return smem + s * X_STAGE + X_A_BYTES; };
-  auto B_of = [&](int s) { return smem + s * X_STAGE + 2 * X_A_BYTES; };
-  auto Blo_of = [&](int s) {
-    return smem + s * X_STAGE + 2 * X_A_BYTES + X_B_BYTES;
-  };
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = cluster_rank();
-  const int cl = int(blockIdx.x >> 1);
   // K-major A: A_lo lives in tensor memory after the accumulator, so only
   // one accumulator fits (the epilogue of a tile holds up the next tile's
   // MMAs); otherwise two accumulators let them overlap.
   constexpr bool kLoTmem = OA == 0;
   constexpr int kAccs = kLoTmem ? 1 : 2;
+  // Without A_lo in shared memory a stage is 48 KiB and four fit where
+  // three of 64 KiB did: a deeper ring for the same bytes.
+  constexpr int kStageBytes = kLoTmem ? X_STAGE - X_A_BYTES : X_STAGE;
+  constexpr int kStages = kLoTmem ? 4 : 3;
+  static_assert(kStages * kStageBytes <= XSTAGES * X_STAGE, "ring fits");
+  static_assert(P_ALO_COL + kStages * XK <= P_TMEM_COLS, "A_lo fits");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* stg0 = smem + kStages * kStageBytes;  // epilogue staging
+  uint8_t* ctrl = stg0 + P_STG_BYTES;
+  const uint32_t full0 = smem_u32(ctrl);          // own TMA landed
+  const uint32_t conv0 = full0 + 8 * kStages;     // own split done
+  const uint32_t empty0 = conv0 + 8 * kStages;    // pair MMAs done reading
+  const uint32_t peer0 = empty0 + 8 * kStages;    // odd block split (even)
+  const uint32_t accf0 = peer0 + 8 * kStages;     // accumulator b complete
+  const uint32_t acce0 = accf0 + 16;              // accumulator b read (even)
+  const uint32_t drain = acce0 + 16;              // teardown (even)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (4 * kStages + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // stage s: A | A_lo (transposed A only) | B | B_lo
+  auto A_of = [&](int s) { return smem + s * kStageBytes; };
+  auto Alo_of = [&](int s) { return smem + s * kStageBytes + X_A_BYTES; };
+  auto B_of = [&](int s) { return A_of(s) + kStageBytes - 2 * X_B_BYTES; };
+  auto Blo_of = [&](int s) { return A_of(s) + kStageBytes - X_B_BYTES; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const int cl = int(blockIdx.x >> 1);
 
   if (tid == 0) {
-    for (int s = 0; s < XSTAGES; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(conv0 + 8 * s, P_CONV_WARPS);
       mbar_init(empty0 + 8 * s, 1);
@@ -782,9 +787,9 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
         const int za = p.bt.a_batched ? item : 0;
         const int zb = p.bt.b_batched ? item : 0;
         for (int k = w.kb; k < w.ke; ++k, ++g) {
-          const int s = g % XSTAGES;
-          if (g >= XSTAGES &&
-              !mbar_wait_bounded(empty0 + 8 * s, ((g / XSTAGES) - 1) & 1,
+          const int s = g % kStages;
+          if (g >= kStages &&
+              !mbar_wait_bounded(empty0 + 8 * s, ((g / kStages) - 1) & 1,
                                  p.status, kSiteTf32Empty, kWaitLimitNs)) {
             *abort_flag = 1;
             break;
@@ -802,8 +807,8 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       }
       // Let the last loads land before the block can exit (they complete
       // even when nobody consumes them).
-      for (int d = g - XSTAGES < 0 ? 0 : g - XSTAGES; d < g; ++d)
-        mbar_wait_bounded(full0 + 8 * (d % XSTAGES), (d / XSTAGES) & 1,
+      for (int d = g - kStages < 0 ? 0 : g - kStages; d < g; ++d)
+        mbar_wait_bounded(full0 + 8 * (d % kStages), (d / kStages) & 1,
                           p.status, kSiteTf32Full, kWaitLimitNs / 100);
     }
   } else if (warp == 1) {
@@ -830,8 +835,8 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
         tc::fence_after_sync();
         const uint32_t acc = tmem + uint32_t(b * P_ACC_COLS);
         for (int k = w.kb; k < w.ke; ++k, ++g) {
-          const int s = g % XSTAGES;
-          const uint32_t par = (g / XSTAGES) & 1;
+          const int s = g % kStages;
+          const uint32_t par = (g / kStages) & 1;
           if (*abort_flag ||
               !mbar_wait_bounded(conv0 + 8 * s, par, p.status, kSiteTf32Conv,
                                  kWaitLimitNs) ||
@@ -880,9 +885,9 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       Unit w;
       for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
         for (int k = w.kb; k < w.ke; ++k, ++g) {
-          const int s = g % XSTAGES;
+          const int s = g % kStages;
           if (*abort_flag ||
-              !mbar_wait_bounded(conv0 + 8 * s, (g / XSTAGES) & 1, p.status,
+              !mbar_wait_bounded(conv0 + 8 * s, (g / kStages) & 1, p.status,
                                  kSiteTf32Conv, kWaitLimitNs)) {
             *abort_flag = 1;
             break;
@@ -905,9 +910,9 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
     // (bar.red), so neither can leave the other waiting at a named barrier.
     for (int u = 0; ok && unit_of(cl, u, p, w); ++u) {
       for (int k = w.kb; k < w.ke; ++k, ++g) {
-        const int s = g % XSTAGES;
+        const int s = g % kStages;
         ok = !*abort_flag &&
-             mbar_wait_bounded(full0 + 8 * s, (g / XSTAGES) & 1, p.status,
+             mbar_wait_bounded(full0 + 8 * s, (g / kStages) & 1, p.status,
                                kSiteTf32Full, kWaitLimitNs);
         ok = named_all(bar_id, 64, ok);
         if (!ok) {
