@@ -162,6 +162,10 @@ cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s);
 // out (cols x rows, dense, ld = rows) = in (rows x cols, ld) transposed.
 cudaError_t launch_transpose(const float* in, int64_t ld, int64_t rows,
                              int64_t cols, float* out, cudaStream_t s);
+// dst (rows x cols, ld dld) = src (rows x cols, ld sld).
+cudaError_t launch_repack(const float* src, int64_t sld, int64_t rows,
+                          int64_t cols, float* dst, int64_t dld,
+                          cudaStream_t s);
 // C = beta * C over M x N (beta == 0: zeros, C not read).
 cudaError_t launch_scale_c(float* C, int64_t ldc, int64_t M, int64_t N,
                            float beta, cudaStream_t s);

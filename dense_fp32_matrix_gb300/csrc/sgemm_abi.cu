@@ -26,6 +26,9 @@ std::atomic<int> g_math_mode{SGEMM_MATH_AUTO};
 // kernel (which splits K over all SMs) beats one tensor-core block per tile.
 constexpr int64_t kTf32MinTiles = 64;
 constexpr int64_t kTf32LongK = 2048;
+// Misaligned operands: repacked for the tensor path from this many
+// multiply-adds on (below, the CUDA-core kernel that reads them as they are).
+constexpr int64_t kTf32RepackMinMacs = int64_t(1) << 24;
 // From this many 256 x 256 tiles on, the 2-SM pair kernel beats the 1-SM one.
 constexpr int64_t kTf32PairMinTiles = 32;
 // Largest M, N or K the int-indexed kernels accept (tile rounding included).
@@ -437,9 +440,15 @@ int plan_call(const Call& c) {
   if (c.N == 1) return SGEMM_PATH_GEMV_COL;
   const int64_t tiles = ((c.M + kTileM - 1) / kTileM) *
                         ((c.N + kTileN - 1) / kTileN);
-  if (tma_operand_ok(a, c.lda) && tma_operand_ok(b, c.ldb) &&
+  // Operands the tensor maps cannot take (row stride or base not 16-byte
+  // aligned) are repacked first when the product is large enough to pay
+  // for the extra pass over them.
+  const bool aligned = tma_operand_ok(a, c.lda) && tma_operand_ok(b, c.ldb);
+  const bool repack_pays =
+      double(c.M) * double(c.N) * double(c.K) >= double(kTf32RepackMinMacs);
+  if ((aligned || repack_pays) &&
       g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO &&
-      !(tiles < kTf32MinTiles && c.K >= kTf32LongK)) {
+      !(aligned && tiles < kTf32MinTiles && c.K >= kTf32LongK)) {
     const int64_t pair_tiles = ((c.M + 255) / 256) * ((c.N + 255) / 256);
     return pair_tiles >= kTf32PairMinTiles ? SGEMM_PATH_TF32X3_PAIR
                                            : SGEMM_PATH_TF32X3;
@@ -490,6 +499,39 @@ int make_row_major(GemmArgs& g, DeviceState& st, cudaStream_t s) {
   return SGEMM_OK;
 }
 
+// Give the tensor maps operands they can take: each operand whose base or
+// row stride is not 16-byte aligned is copied (as stored, op unchanged)
+// into the workspace of stream s with its row stride rounded up to 4
+// floats (st.ws_mu held).
+int make_tensor_ready(GemmArgs& g, DeviceState& st, cudaStream_t s) {
+  const bool a_ok = tma_operand_ok(reinterpret_cast<uint64_t>(g.A), g.lda);
+  const bool b_ok = tma_operand_ok(reinterpret_cast<uint64_t>(g.B), g.ldb);
+  if (a_ok && b_ok) return SGEMM_OK;
+  const int64_t ar = g.op_a ? g.K : g.M, ac = g.op_a ? g.M : g.K;
+  const int64_t br = g.op_b ? g.N : g.K, bc = g.op_b ? g.K : g.N;
+  const int64_t ald = (ac + 3) / 4 * 4, bld = (bc + 3) / 4 * 4;
+  const size_t a_floats = a_ok ? 0 : (size_t(ar) * size_t(ald) + 63) / 64 * 64;
+  const size_t b_floats = b_ok ? 0 : size_t(br) * size_t(bld);
+  Workspace* w = nullptr;
+  int rc = ensure_workspace(st, s, 0, 0, &w);
+  if (rc == SGEMM_OK) rc = ensure_tr(*w, a_floats + b_floats);
+  if (rc != SGEMM_OK) return rc;
+  if (!a_ok) {
+    rc = to_status(launch_repack(g.A, g.lda, ar, ac, w->tr, ald, s));
+    if (rc != SGEMM_OK) return rc;
+    g.A = w->tr;
+    g.lda = ald;
+  }
+  if (!b_ok) {
+    rc = to_status(launch_repack(g.B, g.ldb, br, bc, w->tr + a_floats, bld,
+                                 s));
+    if (rc != SGEMM_OK) return rc;
+    g.B = w->tr + a_floats;
+    g.ldb = bld;
+  }
+  return SGEMM_OK;
+}
+
 int run_call(const Call& call, void* stream, int path) {
   int rc = check_call(call);
   if (rc != SGEMM_OK) return rc;
@@ -519,14 +561,12 @@ int run_call(const Call& call, void* stream, int path) {
   g.sc.beta = call.beta;
   g.op_a = call.op_a;
   g.op_b = call.op_b;
-  const uint64_t a = reinterpret_cast<uint64_t>(call.A);
-  const uint64_t b = reinterpret_cast<uint64_t>(call.B);
   std::lock_guard<std::mutex> lock(st->ws_mu);  // workspace of stream s
   switch (path) {
     case SGEMM_PATH_TF32X3:
     case SGEMM_PATH_TF32X3_PAIR:
-      if (!tma_operand_ok(a, call.lda) || !tma_operand_ok(b, call.ldb))
-        return SGEMM_ERR_PATH;
+      rc = make_tensor_ready(g, *st, s);
+      if (rc != SGEMM_OK) return rc;
       return run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR);
     case SGEMM_PATH_GEMV_COL: {
       if (call.M == 1 && call.N != 1 && call.op_b) {

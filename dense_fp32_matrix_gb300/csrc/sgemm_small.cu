@@ -191,6 +191,18 @@ k_transpose(const float* __restrict__ in, long long ld, int rows, int cols,
   }
 }
 
+// dst (rows x cols, ld dld) = src (rows x cols, ld sld): a repack with
+// another leading dimension. Row-wise grid-stride copy, coalesced on both
+// sides; the padding of dst is not written.
+__global__ void k_repack(const float* __restrict__ src, long long sld,
+                         int rows, int cols, float* __restrict__ dst,
+                         long long dld) {
+  for (long long r = blockIdx.y; r < rows; r += gridDim.y)
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols;
+         c += gridDim.x * blockDim.x)
+      dst[r * dld + c] = src[r * sld + c];
+}
+
 // C = beta * C (beta == 0: C = 0 without reading it).
 __global__ void k_scale_c(float* __restrict__ C, long long ldc, int M, int N,
                           float beta) {
@@ -270,6 +282,18 @@ cudaError_t launch_transpose(const float* in, int64_t ld, int64_t rows,
                   unsigned(row_tiles < 65535 ? row_tiles : 65535));
   k_transpose<<<grid, dim3(TR_TILE, TR_ROWS), 0, s>>>(in, (long long)ld,
                                                       int(rows), int(cols), out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack(const float* src, int64_t sld, int64_t rows,
+                          int64_t cols, float* dst, int64_t dld,
+                          cudaStream_t s) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int64_t gx = (cols + 255) / 256;
+  const dim3 grid(unsigned(gx < 64 ? gx : 64),
+                  unsigned(rows < 65535 ? rows : 65535));
+  k_repack<<<grid, 256, 0, s>>>(src, (long long)sld, int(rows), int(cols), dst,
+                                (long long)dld);
   return cudaGetLastError();
 }
 

@@ -70,9 +70,10 @@ C16 = 0x7f0020000000
     (1024, 1024, 1024, 1024, 1024, 1024, A16, B16, "tf32x3"),
     (2048, 2048, 2048, 2048, 2048, 2048, A16, B16, "tf32x3_pair"),
     (512, 512, 4096, 4096, 512, 512, A16, B16, "tiled_tma"),  # few tiles, long K
-    (4095, 4097, 1023, 1023, 4097, 4097, A16, B16, "tiled_ldg"),  # ld % 4
-    (127, 129, 33, 33, 129, 129, A16, B16, "tiled_ldg"),
-    (4096, 4096, 4096, 4096, 4096, 4096, A16 + 4, B16, "tiled_ldg"),  # align
+    # ld % 4 != 0: repacked for the tensor path (large enough)
+    (4095, 4097, 1023, 1023, 4097, 4097, A16, B16, "tf32x3_pair"),
+    (127, 129, 33, 33, 129, 129, A16, B16, "tiled_ldg"),  # too small to repack
+    (4096, 4096, 4096, 4096, 4096, 4096, A16 + 4, B16, "tf32x3_pair"),  # align
     (4096, 4096, 4096, 4100, 4096, 4096, A16, B16, "tf32x3_pair"),  # pitch
     (1, 4096, 4096, 4096, 4096, 4096, A16, B16, "gemv_row"),
     (4096, 1, 4096, 4096, 1, 1, A16, B16, "gemv_col"),
@@ -139,11 +140,10 @@ def test_sgemm_rejects_bad_arguments_before_touching_a_device(lib):
     ("N", "T", 4096, 4096, 4096, 4096, 4096, A16, B16, "tf32x3_pair"),
     ("T", "N", 4096, 4096, 4096, 4096, 4096, A16, B16, "tf32x3_pair"),
     ("T", "T", 512, 384, 256, 512, 256, A16, B16, "tf32x3"),
-    # lda % 4 != 0 rules out the tensor path; A^T is copied row-major
-    # (dense, ld = K) for the FFMA tile kernel
-    ("T", "N", 4096, 4096, 4096, 4097, 4096, A16, B16, "tiled_tma"),
-    # A misaligned as given: the cp.async tile kernel (B^T copied row-major)
-    ("N", "T", 300, 200, 64, 64, 64, A16 + 4, B16, "tiled_ldg"),
+    # lda % 4 != 0: A repacked (as stored) for the tensor path
+    ("T", "N", 4096, 4096, 4096, 4097, 4096, A16, B16, "tf32x3_pair"),
+    # A misaligned and too small to repack: the cp.async tile kernel
+    ("N", "T", 100, 20, 64, 64, 64, A16 + 4, B16, "tiled_ldg"),
     ("N", "T", 1, 4096, 4096, 4096, 4096, A16, B16, "gemv_col"),  # a * B^T
     ("T", "N", 1, 4096, 4096, 1, 4096, A16, B16, "gemv_row"),
     ("T", "N", 4096, 1, 4096, 4096, 1, A16, B16, "gemv_col"),

@@ -61,15 +61,14 @@ def test_pitch_padding_never_read_or_written(path):
     run_case(260, 132, 36, "integers", 9, lda=40, ldb=136, ldc=133, path=path)
 
 
-def test_unaligned_layout_is_refused():
-    import torch
-    import dense_fp32_matrix_gb300 as dfm
-    buf = torch.zeros(1 << 16, device="cuda")
-    p = buf.data_ptr()
-    with pytest.raises(dfm.SgemmError) as e:
-        dfm.sgemm_path(64, 64, 33, p, 33, p + 4 * 8192, 64, p + 4 * 32768, 64,
-                       path=PATH)
-    assert e.value.status == dfm.STATUS["SGEMM_ERR_PATH"]
+@pytest.mark.parametrize("path", [PATH, PAIR])
+def test_misaligned_operands_are_repacked(path):
+    # Row strides or bases that are not 16-byte aligned are copied with an
+    # aligned stride before the tensor maps are made (same results bar).
+    run_case(64, 64, 33, "integers", 3, path=path, check="full")
+    run_case(300, 260, 101, "uniform", 4, lda=103, ldb=263, ldc=261, path=path)
+    run_case(257, 130, 77, "integers", 5, path=path, offsets=(1, 3, 2))
+    run_case(1000, 1030, 513, "uniform", 6, path="auto", offsets=(1, 1, 1))
 
 
 def test_nan_and_inf_propagate():
