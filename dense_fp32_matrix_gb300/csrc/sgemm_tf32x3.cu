@@ -639,40 +639,53 @@ __device__ __forceinline__ bool unit_of(int c, int u, const PairParams& p,
 
 // Stores one lane-quarter's 32 rows x 256 columns of C from accumulator
 // columns `acc` (rows m0 + lane, columns n0 ..).
-__device__ __forceinline__ void store_c_quarter(uint32_t acc, float* crow,
-                                                bool row_ok, int n0,
-                                                const PairParams& p) {
+// Direct stores of C (beta != 0, C not 16-byte aligned, stream-K fix-up)
+// also go through the warp's staging box, so that they are coalesced rows:
+// each lane stages its row (32 values, 128-byte swizzle), then the warp
+// writes the box back row by row with lane j on column j (one 128-byte
+// row per instruction; the old C is read the same way when beta != 0).
+// rows / cols: the box's part inside C.
+__device__ __forceinline__ void write_box_rows(const uint8_t* box, float* c0,
+                                               long long ldc, int rows,
+                                               int cols, int lane,
+                                               const Scale& sc) {
+  if (lane >= cols) return;
+  const int w = lane >> 2, b = (lane & 3) * 4;
+#pragma unroll 1
+  for (int rr = 0; rr < rows; ++rr) {
+    const float x = *reinterpret_cast<const float*>(
+        box + rr * 128 + ((w ^ (rr & 7)) << 4) + b);
+    float* dst = c0 + rr * ldc + lane;
+    *dst = epi1(x, dst, sc);
+  }
+}
+
+// One lane quarter's 32 rows x 256 columns of C from accumulator columns
+// `acc`, written through the staging box; cq = C at the quarter's first row
+// and the tile's first column.
+__device__ __forceinline__ void store_c_staged(uint32_t acc, uint8_t* box,
+                                               float* cq, long long ldc,
+                                               int rows, int cols, int lane,
+                                               const Scale& sc) {
+  if (lane == 0) bulk_wait_group_read<0>();  // box free of bulk stores
 #pragma unroll 1
   for (int cb = 0; cb < PN / 32; ++cb) {
     uint32_t v[32];
     tc::tmem_ld_32x32b_x32(acc + 32 * cb, v);
     tc::tmem_ld_wait();
-    if (!row_ok) continue;
-    const int c0 = n0 + 32 * cb;
+    __syncwarp();  // the previous box's rows have been written out
 #pragma unroll
-    for (int e = 0; e < 32; e += 4) {
-      const int c = c0 + e;
-      if (p.vec_store && c + 3 < p.N) {
-        *reinterpret_cast<float4*>(crow + c) = epi4(
-            make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])),
-            crow + c, p.sc);
-      } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (c + u < p.N)
-            crow[c + u] = epi1(__uint_as_float(v[e + u]), crow + c + u, p.sc);
-      }
-    }
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<float4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+          make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                      __uint_as_float(v[4 * c + 2]),
+                      __uint_as_float(v[4 * c + 3]));
+    __syncwarp();
+    write_box_rows(box, cq + 32 * cb, ldc, rows,
+                   cols - 32 * cb < 32 ? cols - 32 * cb : 32, lane, sc);
   }
 }
 
-// One lane quarter's 32 rows x 256 columns of C from accumulator columns
-// `acc` through the warp's two staging boxes and bulk tensor stores (the
-// store clips rows >= M and columns >= N). Each lane writes its row of a
-// 32 x 32 box with the 128-byte swizzle (16-byte chunk c of row r at
-// c ^ (r & 7): conflict-free), then lane 0 stores the box. A box is reused
-// once the store issued from it two boxes earlier has read it.
 // One lane quarter's 32 rows x 256 columns of C from accumulator columns
 // `acc` through the warp's two staging boxes and bulk tensor stores (the
 // store clips rows >= M and columns >= N). Each lane writes its row of a
@@ -953,16 +966,17 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
                            (uint32_t(32 * quarter) << 16);
       int item, pm, pn;
       pair_tile(w.tile, p, item, pm, pn);
-      const int r = pm * PM + 128 * int(rank) + row;
       const int n0 = pn * PN;
-      float* crow = p.C + item * p.bt.stride_c + (long long)r * p.ldc;
+      const int r0q = pm * PM + 128 * int(rank) + 32 * quarter;
+      float* cq = p.C + item * p.bt.stride_c + (long long)r0q * p.ldc + n0;
+      const int rows_in = p.M - r0q < 32 ? p.M - r0q : 32;
+      const int cols_in = p.N - n0 < PN ? p.N - n0 : PN;
+      uint8_t* stg = stg0 + (warp - P_EPI_WARP0) * 2 * P_STG_BOX;
       int slot = 0;
       if (w.sk < 0 && p.tma_c) {
-        store_c_tma(acc, stg0 + (warp - P_EPI_WARP0) * 2 * P_STG_BOX, &tmC,
-                    lane, n0, pm * PM + 128 * int(rank) + 32 * quarter, item,
-                    p.sc.alpha);
+        store_c_tma(acc, stg, &tmC, lane, n0, r0q, item, p.sc.alpha);
       } else if (w.sk < 0) {
-        store_c_quarter(acc, crow, r < p.M, n0, p);
+        store_c_staged(acc, stg, cq, p.ldc, rows_in, cols_in, lane, p.sc);
       } else {
         // this block's piece: thread-major float4s, coalesced per warp
         const long long x0 = (long long)w.sk * p.T;
@@ -1005,42 +1019,42 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       const int pieces = sk_owner(x0 + p.T - 1, p) - c_first + 1;
       if (arrived != pieces - 1) continue;
       __threadfence();
-      const bool row_ok = r < p.M;
+      if (lane == 0) bulk_wait_group_read<0>();  // box free of bulk stores
 #pragma unroll 1
       for (int cb = 0; cb < PN / 32; ++cb) {
-        float4 sum[8];
-        for (int j = 0; j < pieces; ++j) {
-          const int cj = c_first + j;
-          const int sj = sk_begin(cj, p) >= x0 ? 0 : 1;
-          const float4* pj = ws4 + ((long long)(cj * 2 + sj) * 2 + rank) *
-                                       (P_PIECE_FLOATS / 4);
+        __syncwarp();  // the previous box's rows have been written out
+        // two halves of 16 columns (fewer live registers); each sum adds
+        // the pieces in piece order (k order)
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          float4 sum[4];
+          for (int j = 0; j < pieces; ++j) {
+            const int cj = c_first + j;
+            const int sj = sk_begin(cj, p) >= x0 ? 0 : 1;
+            const float4* pj = ws4 + ((long long)(cj * 2 + sj) * 2 + rank) *
+                                         (P_PIECE_FLOATS / 4);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 x = __ldcg(pj + (cb * 8 + e) * 128 + row);
-            if (j == 0) {
-              sum[e] = x;
-            } else {
-              sum[e].x += x.x;
-              sum[e].y += x.y;
-              sum[e].z += x.z;
-              sum[e].w += x.w;
+            for (int e = 0; e < 4; ++e) {
+              const float4 x = __ldcg(pj + (cb * 8 + 4 * h + e) * 128 + row);
+              if (j == 0) {
+                sum[e] = x;
+              } else {
+                sum[e].x += x.x;
+                sum[e].y += x.y;
+                sum[e].z += x.z;
+                sum[e].w += x.w;
+              }
             }
           }
-        }
-        if (!row_ok) continue;
-        const int c0 = n0 + 32 * cb;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = c0 + 4 * e;
-          if (p.vec_store && c + 3 < p.N) {
-            *reinterpret_cast<float4*>(crow + c) = epi4(sum[e], crow + c, p.sc);
-          } else {
-            const float s4[4] = {sum[e].x, sum[e].y, sum[e].z, sum[e].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (c + q < p.N) crow[c + q] = epi1(s4[q], crow + c + q, p.sc);
-          }
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<float4*>(
+                stg + lane * 128 + (((4 * h + e) ^ (lane & 7)) << 4)) = sum[e];
         }
+        __syncwarp();
+        write_box_rows(stg, cq + 32 * cb, p.ldc, rows_in,
+                       cols_in - 32 * cb < 32 ? cols_in - 32 * cb : 32, lane,
+                       p.sc);
       }
       if (lane == 0) *counter = 0;
     }
