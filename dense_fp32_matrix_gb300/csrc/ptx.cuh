@@ -32,6 +32,7 @@ enum WaitSite : int {
   kSiteTf32Empty = 8,
   kSiteTf32Acc = 9,
   kSiteTf32Peer = 10,
+  kSiteTf32Fix = 11,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -249,6 +250,29 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src,
                                            uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst),
                "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// global -> this CTA's shared memory, completion as transaction bytes on
+// the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
+                                          uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared, cached in L2 only.
+__device__ __forceinline__ void cp_async_16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+               "l"(src)
                : "memory");
 }
 

@@ -482,6 +482,12 @@ constexpr int P_PIECE_FLOATS = 128 * PN;             // one block's half tile
 // 4 KiB boxes of 32 rows x 32 columns (128-byte rows, 128-byte swizzle).
 constexpr int P_STG_BOX = 32 * 32 * 4;
 constexpr int P_STG_BYTES = 4 * 2 * P_STG_BOX;       // 32 KiB
+// Stream-K fix-ups reuse the stage ring: per epilogue warp 48 KiB, 11
+// slots of 4 KiB and their mbarriers.
+constexpr int kFixSlots = 11;
+constexpr int kFixRegion = 48 * 1024;
+static_assert(kFixSlots * P_STG_BOX + 8 * kFixSlots <= kFixRegion, "slots");
+static_assert(4 * kFixRegion <= XSTAGES * X_STAGE, "fix-up regions");
 constexpr size_t P_SMEM =
     size_t(XSTAGES) * X_STAGE + P_STG_BYTES + 1024 + 256;
 static_assert(P_SMEM <= 232448, "shared memory per block");
@@ -651,12 +657,28 @@ __device__ __forceinline__ void write_box_rows(const uint8_t* box, float* c0,
                                                const Scale& sc) {
   if (lane >= cols) return;
   const int w = lane >> 2, b = (lane & 3) * 4;
+  // 8 rows per round: their loads (box, and the old C when beta != 0) are
+  // issued before their stores.
 #pragma unroll 1
-  for (int rr = 0; rr < rows; ++rr) {
-    const float x = *reinterpret_cast<const float*>(
-        box + rr * 128 + ((w ^ (rr & 7)) << 4) + b);
-    float* dst = c0 + rr * ldc + lane;
-    *dst = epi1(x, dst, sc);
+  for (int r0 = 0; r0 < rows; r0 += 8) {
+    float x[8], y[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int rr = r0 + u;
+      x[u] = 0.f;
+      y[u] = 0.f;
+      if (rr < rows) {
+        x[u] = *reinterpret_cast<const float*>(
+            box + rr * 128 + ((w ^ (rr & 7)) << 4) + b);
+        if (sc.beta != 0.f) y[u] = c0[rr * ldc + lane];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (r0 + u < rows)
+        c0[(r0 + u) * ldc + lane] = sc.beta == 0.f
+                                        ? sc.alpha * x[u]
+                                        : fmaf(sc.alpha, x[u], sc.beta * y[u]);
   }
 }
 
@@ -953,6 +975,11 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
     const int row = 32 * quarter + lane;  // row within the block's half
     const uint32_t acce_leader = cluster_map(acce0, 0);
     float4* ws4 = reinterpret_cast<float4*>(p.ws);
+    // Stream-K tiles whose pieces this warp sums (a cluster's share of
+    // split k-slices has at most two partial segments).
+    constexpr int kMaxFix = 2;
+    int fix_tile[kMaxFix];
+    int nfix = 0;
     Unit w;
     for (int u = 0; !*abort_flag && unit_of(cl, u, p, w); ++u) {
       const int b = u % kAccs;
@@ -978,11 +1005,15 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       } else if (w.sk < 0) {
         store_c_staged(acc, stg, cq, p.ldc, rows_in, cols_in, lane, p.sc);
       } else {
-        // this block's piece: thread-major float4s, coalesced per warp
+        // this block's piece, warp-major: lane quarter q's column block cb
+        // is 4 KiB at float4 (q * 8 + cb) * 256, element (e, lane) at
+        // e * 32 + lane (stores coalesced per warp; one bulk copy per block
+        // for the fix-up)
         const long long x0 = (long long)w.sk * p.T;
         slot = sk_begin(cl, p) >= x0 ? 0 : 1;
         float4* piece = ws4 + ((long long)(cl * 2 + slot) * 2 + rank) *
-                                  (P_PIECE_FLOATS / 4);
+                                  (P_PIECE_FLOATS / 4) +
+                        quarter * 8 * 256 + lane;
 #pragma unroll 1
         for (int cb = 0; cb < PN / 32; ++cb) {
           uint32_t v[32];
@@ -990,7 +1021,7 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
           tc::tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            __stcg(piece + (cb * 8 + e) * 128 + row,
+            __stcg(piece + (cb * 8 + e) * 32,
                    make_float4(__uint_as_float(v[4 * e]),
                                __uint_as_float(v[4 * e + 1]),
                                __uint_as_float(v[4 * e + 2]),
@@ -1019,44 +1050,139 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       const int pieces = sk_owner(x0 + p.T - 1, p) - c_first + 1;
       if (arrived != pieces - 1) continue;
       __threadfence();
-      if (lane == 0) bulk_wait_group_read<0>();  // box free of bulk stores
+      // the last piece in: sum the pieces once this warp's own units are
+      // done (then the stage buffers are free for a deep copy pipeline)
+      if (nfix < kMaxFix) fix_tile[nfix++] = w.tile;
+
+    }
+    // ------------------------------------------------ stream-K fix-ups
+    // All MMAs of this cluster have completed (its last accumulator is
+    // in), so the stage ring is free: each epilogue warp streams the
+    // pieces through 12 slots of 4 KiB of it with cp.async (11 chunks in
+    // flight), every lane its own row, and adds them into the staging box
+    // in piece (k) order; a finished box goes out as coalesced rows.
+    if (lane == 0) bulk_wait_group_read<0>();  // boxes free of bulk stores
+    __syncwarp();
+    for (int f = 0; f < nfix && !*abort_flag; ++f) {
+      int item, pm, pn;
+      pair_tile(fix_tile[f], p, item, pm, pn);
+      const int sk = fix_tile[f] - p.dp_tiles;
+      const long long x0 = (long long)sk * p.T;
+      const int c_first = sk_owner(x0, p);
+      const int pieces = sk_owner(x0 + p.T - 1, p) - c_first + 1;
+      const int n0 = pn * PN;
+      const int r0q = pm * PM + 128 * int(rank) + 32 * quarter;
+      float* cq = p.C + item * p.bt.stride_c + (long long)r0q * p.ldc + n0;
+      const int rows_in = p.M - r0q < 32 ? p.M - r0q : 32;
+      const int cols_in = p.N - n0 < PN ? p.N - n0 : PN;
+      uint8_t* stg = stg0 + (warp - P_EPI_WARP0) * 2 * P_STG_BOX;
+      uint8_t* slots = smem + (warp - P_EPI_WARP0) * kFixRegion;
+      // Piece of contributor j: only the first contributor's share can
+      // start before the tile, so only its piece can be its second slot.
+      const int s_first = sk_begin(c_first, p) >= x0 ? 0 : 1;
+      auto piece = [&](int j) {
+        return ws4 + ((long long)((c_first + j) * 2 + (j == 0 ? s_first : 0)) *
+                          2 + rank) * (P_PIECE_FLOATS / 4) + quarter * 8 * 256;
+      };
+      // Chunk (column block icb, piece ij) = 4 KiB, one bulk copy by lane 0
+      // into slot islot, completing on that slot's mbarrier.
+      const uint32_t bar0 = smem_u32(slots + kFixSlots * P_STG_BOX);
+      if (lane == 0) {
+        for (int i = 0; i < kFixSlots; ++i) mbar_init(bar0 + 8 * i, 1);
+        mbar_fence_init();
+        // the other blocks' piece stores (generic) before the bulk reads
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      __syncwarp();
+      const int nb = pieces * (PN / 32);
+      int icb = 0, ij = 0, issued = 0;
+      auto issue_next = [&]() {
+        if (issued < nb) {
+          if (lane == 0) {
+            const int sl = issued % kFixSlots;
+            mbar_arrive_expect_tx(bar0 + 8 * sl, P_STG_BOX);
+            bulk_load(smem_u32(slots + sl * P_STG_BOX), piece(ij) + icb * 256,
+                      P_STG_BOX, bar0 + 8 * sl);
+          }
+          if (++ij == pieces) {
+            ij = 0;
+            ++icb;
+          }
+          ++issued;
+        }
+      };
+      for (int t = 0; t < kFixSlots; ++t) issue_next();
+      bool fix_ok = true;
+      int t = 0;
 #pragma unroll 1
-      for (int cb = 0; cb < PN / 32; ++cb) {
-        __syncwarp();  // the previous box's rows have been written out
-        // two halves of 16 columns (fewer live registers); each sum adds
-        // the pieces in piece order (k order)
+      for (int cb = 0; cb < PN / 32 && fix_ok; ++cb) {
+        float4 acc[8];
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          float4 sum[4];
-          for (int j = 0; j < pieces; ++j) {
-            const int cj = c_first + j;
-            const int sj = sk_begin(cj, p) >= x0 ? 0 : 1;
-            const float4* pj = ws4 + ((long long)(cj * 2 + sj) * 2 + rank) *
-                                         (P_PIECE_FLOATS / 4);
+        for (int j = 0; j < pieces; ++j, ++t) {
+          const int sl = t % kFixSlots;
+          fix_ok = mbar_wait_bounded(bar0 + 8 * sl, (t / kFixSlots) & 1,
+                                     p.status, kSiteTf32Fix, kWaitLimitNs);
+          fix_ok = __all_sync(0xffffffffu, fix_ok);
+          if (!fix_ok) break;
+          const float4* slot4 =
+              reinterpret_cast<const float4*>(slots + sl * P_STG_BOX) + lane;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float4 x = __ldcg(pj + (cb * 8 + 4 * h + e) * 128 + row);
-              if (j == 0) {
-                sum[e] = x;
-              } else {
-                sum[e].x += x.x;
-                sum[e].y += x.y;
-                sum[e].z += x.z;
-                sum[e].w += x.w;
-              }
+          for (int e = 0; e < 8; ++e) {
+            const float4 x = slot4[e * 32];
+            if (j == 0) {
+              acc[e] = x;
+            } else {
+              acc[e].x += x.x;
+              acc[e].y += x.y;
+              acc[e].z += x.z;
+              acc[e].w += x.w;
             }
           }
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<float4*>(
-                stg + lane * 128 + (((4 * h + e) ^ (lane & 7)) << 4)) = sum[e];
+          __syncwarp();   // every lane has read the slot ...
+          issue_next();   // ... before it is refilled
         }
+        if (!fix_ok) break;
+        if (p.tma_c) {
+          // bulk tensor store of the block (the two boxes alternate; a box
+          // is rewritten once the store issued from it has read it)
+          uint8_t* box = stg + (cb & 1) * P_STG_BOX;
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<float4*>(box + lane * 128 +
+                                       ((e ^ (lane & 7)) << 4)) =
+                make_float4(p.sc.alpha * acc[e].x, p.sc.alpha * acc[e].y,
+                            p.sc.alpha * acc[e].z, p.sc.alpha * acc[e].w);
+          fence_async_shared();  // generic writes -> visible to the store
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmC, smem_u32(box), n0 + 32 * cb, r0q, item);
+            bulk_commit_group();
+          }
+          continue;
+        }
+        __syncwarp();  // the previous block's rows have been written out
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<float4*>(stg + lane * 128 + ((e ^ (lane & 7)) << 4)) =
+              acc[e];
         __syncwarp();
         write_box_rows(stg, cq + 32 * cb, p.ldc, rows_in,
                        cols_in - 32 * cb < 32 ? cols_in - 32 * cb : 32, lane,
                        p.sc);
       }
-      if (lane == 0) *counter = 0;
+      if (!fix_ok) *abort_flag = 1;
+      // copies still in flight land before the slots' barriers go away
+      if (lane == 0) {
+        for (int d = t; d < issued; ++d)
+          mbar_wait_bounded(bar0 + 8 * (d % kFixSlots), (d / kFixSlots) & 1,
+                            p.status, kSiteTf32Fix, kWaitLimitNs / 100);
+        for (int i = 0; i < kFixSlots; ++i) mbar_inval(bar0 + 8 * i);
+      }
+      __syncwarp();
+      if (lane == 0)
+        p.counters[(sk * 2 + int(rank)) * 4 + quarter] = 0;
     }
     if (lane == 0) bulk_wait_group_all();  // C stores complete
   }
