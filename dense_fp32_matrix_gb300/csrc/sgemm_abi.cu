@@ -22,15 +22,18 @@ __device__ int g_status[4];
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_math_mode{SGEMM_MATH_AUTO};
-// Below this many 128 x 128 tiles with K this long, the stream-K CUDA-core
-// kernel (which splits K over all SMs) beats one tensor-core block per tile.
-constexpr int64_t kTf32MinTiles = 64;
-constexpr int64_t kTf32LongK = 2048;
 // Misaligned operands: repacked for the tensor path from this many
 // multiply-adds on (below, the CUDA-core kernel that reads them as they are).
 constexpr int64_t kTf32RepackMinMacs = int64_t(1) << 24;
-// From this many 256 x 256 tiles on, the 2-SM pair kernel beats the 1-SM one.
-constexpr int64_t kTf32PairMinTiles = 32;
+// From this much work on (256 x 256 tiles x k-slices of 32) the 2-SM pair
+// kernel, which splits k-slices over all clusters when tiles are few, beats
+// one 1-SM block per 128 x 128 tile (measured: 1024^3 and every long-K
+// shape of few tiles go to pairs, 512^3 stays on single blocks).
+constexpr int64_t kTf32PairMinWork = 256;
+
+int64_t pair_work(int64_t M, int64_t N, int64_t K, int64_t batch) {
+  return batch * ((M + 255) / 256) * ((N + 255) / 256) * ((K + 31) / 32);
+}
 // Largest M, N or K the int-indexed kernels accept (tile rounding included).
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1024;
 
@@ -447,10 +450,9 @@ int plan_call(const Call& c) {
   const bool repack_pays =
       double(c.M) * double(c.N) * double(c.K) >= double(kTf32RepackMinMacs);
   if ((aligned || repack_pays) &&
-      g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO &&
-      !(aligned && tiles < kTf32MinTiles && c.K >= kTf32LongK)) {
-    const int64_t pair_tiles = ((c.M + 255) / 256) * ((c.N + 255) / 256);
-    return pair_tiles >= kTf32PairMinTiles ? SGEMM_PATH_TF32X3_PAIR
+      g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO) {
+    return pair_work(c.M, c.N, c.K, 1) >= kTf32PairMinWork
+               ? SGEMM_PATH_TF32X3_PAIR
                                            : SGEMM_PATH_TF32X3;
   }
   // CUDA-core tile kernels take row-major operands; a transposed one is
@@ -676,7 +678,6 @@ int run_batched(const Call& c, int64_t stride_a, int64_t stride_b,
       return SGEMM_ERR_OVERLAP;
   }
   const bool strides_ok = stride_a % 4 == 0 && stride_b % 4 == 0;
-  const int64_t pair_tiles = ((c.M + 255) / 256) * ((c.N + 255) / 256);
   const int64_t tiles = ((c.M + kTileM - 1) / kTileM) *
                         ((c.N + kTileN - 1) / kTileN);
   const bool tensor_ok =
@@ -687,8 +688,9 @@ int run_batched(const Call& c, int64_t stride_a, int64_t stride_b,
   if (path == SGEMM_PATH_AUTO && tensor_ok &&
       g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO &&
       c.M > 1 && c.N > 1)
-    path = batch * pair_tiles >= kTf32PairMinTiles ? SGEMM_PATH_TF32X3_PAIR
-                                                   : SGEMM_PATH_TF32X3;
+    path = pair_work(c.M, c.N, c.K, batch) >= kTf32PairMinWork
+               ? SGEMM_PATH_TF32X3_PAIR
+               : SGEMM_PATH_TF32X3;
   if (reads_ab(c) &&
       (path == SGEMM_PATH_TF32X3 || path == SGEMM_PATH_TF32X3_PAIR)) {
     if (!tensor_ok) return SGEMM_ERR_PATH;

@@ -67,9 +67,10 @@ C16 = 0x7f0020000000
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc,a,b,expect", [
     (4096, 4096, 4096, 4096, 4096, 4096, A16, B16, "tf32x3_pair"),
     (256, 256, 256, 256, 256, 256, A16, B16, "tf32x3"),
-    (1024, 1024, 1024, 1024, 1024, 1024, A16, B16, "tf32x3"),
+    (1024, 1024, 1024, 1024, 1024, 1024, A16, B16, "tf32x3_pair"),
+    (512, 512, 512, 512, 512, 512, A16, B16, "tf32x3"),
     (2048, 2048, 2048, 2048, 2048, 2048, A16, B16, "tf32x3_pair"),
-    (512, 512, 4096, 4096, 512, 512, A16, B16, "tiled_tma"),  # few tiles, long K
+    (512, 512, 4096, 4096, 512, 512, A16, B16, "tf32x3_pair"),  # long K: split
     # ld % 4 != 0: repacked for the tensor path (large enough)
     (4095, 4097, 1023, 1023, 4097, 4097, A16, B16, "tf32x3_pair"),
     (127, 129, 33, 33, 129, 129, A16, B16, "tiled_ldg"),  # too small to repack
