@@ -220,6 +220,23 @@ def cpu_oracle_rate(M, N, K, kind, seed, target_s=CPU_SAMPLE_SECONDS,
     return flops(rows, N, K) / dt / 1e12, rows, dt, threads
 
 
+def reduce_max(x, world, device="cuda"):
+    """Max over the ranks of a per-rank number (the slowest replica sets the
+    whole-job time); the number itself for one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_rank, ms_max, world):
+    """Whole-job throughput: every rank's flops over the slowest rank's time."""
+    return flop_per_rank * world / (ms_max * 1e-3) / 1e12
+
+
 def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -337,13 +354,9 @@ def run_gpu(args, w):
     if st != 0:
         raise RuntimeError("watchdog fired during timing (site %d)" % site)
     ms = [a.elapsed_time(b) for a, b in ev]
-    ms_step = sum(ms) / len(ms)
-    if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = reduce_max(sum(ms) / len(ms), world)
     tflops = flops(M, N, K) / (ms_step * 1e-3) / 1e12
-    value = tflops * world
+    value = job_tflops(flops(M, N, K), ms_step, world)
     clk = clocks.summary()
 
     # e2e through the C ABI with host buffers: H2D inputs, compute, D2H C.
@@ -371,7 +384,7 @@ def run_gpu(args, w):
         dfm.sgemm_host(M, N, K, hA, K, hB, N, hC, N, dA, dB, dC, stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world)
     dfm.sgemm_set_math_mode(prev_mode)
     # sgemm_host pipelines large products in row blocks, each computed as
     # sgemm of that block, so it may differ from the one-piece product in
@@ -433,9 +446,10 @@ def run_gpu(args, w):
                              args.warmup)
         finally:
             dfm.sgemm_set_math_mode(prev)
-        f_ms = sum(fms) / len(fms)
+        f_ms = reduce_max(sum(fms) / len(fms), world)
         f_tflops = flops(M, N, K) / (f_ms * 1e-3) / 1e12
-        ffma = {"path": ffma_path, "value": f_tflops * world,
+        ffma = {"path": ffma_path, "value": job_tflops(flops(M, N, K), f_ms,
+                                                        world),
                 "ms_per_step": f_ms, "frac_of_ffma_peak": f_tflops / ffma_peak,
                 "traffic": recorded_traffic("k_tiled_tma", w["name"])}
 
@@ -460,7 +474,7 @@ def run_gpu(args, w):
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
                    "reasons": clk["reasons"], "samples": clk["samples"],
                    "power_w_max": clk.get("power_w_max")},
-        "e2e": {"value": flops(M, N, K) / (e2e_ms * 1e-3) / 1e12 * world,
+        "e2e": {"value": job_tflops(flops(M, N, K), e2e_ms, world),
                 "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 4 * (M * K + K * N),
                 "d2h_bytes_per_step": 4 * M * N,
