@@ -4,12 +4,17 @@
 Default workload: M = N = K = 4096, A and B i.i.d. uniform[-1, 1) from seed 1
 (the pages' problem size, "GEMM from naive to tiled", section 二.1). A step
 is one call of the C ABI on device-resident inputs; L2 is flushed (a 256 MiB
-device memset) before every step, outside the timed events. Reported:
+device write, then a 256 MiB read, so that no dirty lines remain) before
+every step, outside the timed events. Reported:
 
   value      TFLOP/s = 2 M N K / mean device time of a step (CUDA events on
              the launching stream), summed over ranks (replicas);
-  roofline   the FP32 FMA-pipe roofline: SMs x 128 FMA/clk x 2 flop x the
-             median SM clock sampled during the timed region ("alu" bound);
+  roofline   the bound of the kernel the step runs: "tensor" for the 3xTF32
+             kernels (the measured bf16 GEMM peak scaled to TF32 and divided
+             by the 3 products per fp32 product), "hbm" for the vector shapes
+             (algorithmic bytes against the measured copy bandwidth), "alu"
+             for the FFMA kernels (SMs x 128 FMA/clk x 2 flop x the median SM
+             clock sampled during the timed region);
   e2e        the same metric through sgemm_host(): pinned host A, B in,
              host C out, copies inside the timed region;
   cpu_baseline  the CPU oracle timed on this host's cores on a bounded row
@@ -39,6 +44,7 @@ CPU_SAMPLE_SECONDS = 12.0
 # Nominal dense tensor rates per GPU: TF32 1.1 PFLOP/s, BF16 2.25 PFLOP/s.
 TF32_PER_BF16 = 1.1 / 2.25
 BF16_FALLBACK_TFLOPS = 1900.0   # used only when no measured peak is present
+HBM_FALLBACK_GBS = 6800.0
 TF32X3_PRODUCTS = 3             # TF32 tensor products per fp32 product
 # Dense TF32 tensor-core rate of one SM, ops per clock, as ncu reports it
 # for this part (the peak_sustained of the TF32 tensor-op counter; see
@@ -61,6 +67,8 @@ KERNEL_SOURCES = {
     "k_tf32x3": ["sgemm_tf32x3.cu", "tcgen05.cuh", "ptx.cuh", "kernels.h"],
     "k_tf32x3_pair": ["sgemm_tf32x3.cu", "tcgen05.cuh", "ptx.cuh",
                       "kernels.h"],
+    "k_gemv_row_tma": ["sgemm_gemv.cu", "ptx.cuh", "kernels.h"],
+    "k_gemv_col_tma": ["sgemm_gemv.cu", "ptx.cuh", "kernels.h"],
 }
 
 
@@ -167,17 +175,45 @@ def measured_bf16_tflops():
         return BF16_FALLBACK_TFLOPS, "fallback"
 
 
+def measured_hbm_gbs():
+    """(HBM copy GB/s, source) from MEASURED_PEAKS.json."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, ValueError, KeyError):
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+class L2Flush:
+    """Evicts the step's inputs from L2 before each step: writes a buffer
+    larger than L2, then reads another one, so that L2 is left holding clean
+    lines and the timed step pays no write-back of the flush's dirty data."""
+
+    def __init__(self):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32,
+                             device="cuda")
+        self.sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=(0,), out=self.sink)
+
+
 def time_steps(step, flush, stream, n, warmup):
     """Per-step device times (ms) with an L2 flush before each step."""
     import torch
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for i in range(n):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -319,7 +355,7 @@ def run_gpu(args, w):
     A = torch.from_numpy(matgen.KINDS[w["kind"]](w["seed"], 0, M, K)).cuda()
     B = torch.from_numpy(matgen.KINDS[w["kind"]](w["seed"], 1, K, N)).cuda()
     C = torch.empty((M, N), device="cuda")
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     stream = torch.cuda.current_stream()
     path_name = args.path
     plan = dfm.sgemm_plan(M, N, K, K, N, N, A.data_ptr(), B.data_ptr(),
@@ -329,7 +365,7 @@ def run_gpu(args, w):
         dfm.sgemm_path(M, N, K, A, K, B, N, C, N, stream, path_name)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     st, site = dfm.sgemm_watchdog_status()
@@ -343,7 +379,7 @@ def run_gpu(args, w):
     torch.cuda.synchronize()
     with ClockSampler(dev) as clocks:
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -402,7 +438,8 @@ def run_gpu(args, w):
                   "clock sampled during the timed region)"
                   % (sms, FMA_PER_CLK_PER_SM, peak_clock_mhz))
     kernel = {"tiled_tma": "k_tiled_tma", "tiled_ldg": "k_tiled_ldg",
-              "tf32x3": "k_tf32x3", "tf32x3_pair": "k_tf32x3_pair"}.get(
+              "tf32x3": "k_tf32x3", "tf32x3_pair": "k_tf32x3_pair",
+              "gemv_row": "k_gemv_row_tma", "gemv_col": "k_gemv_col_tma"}.get(
                   plan, plan)
     if plan.startswith("tf32x3"):
         bf16, src = measured_bf16_tflops()
@@ -429,6 +466,17 @@ def run_gpu(args, w):
             "frac": TF32X3_PRODUCTS * tflops / hw_peak,
             "basis": ("%d SMs x %d dense TF32 ops/clk (ncu) x %.0f MHz"
                       % (sms, TF32_OPS_PER_CLK_PER_SM, peak_clock_mhz))}
+    elif plan in ("gemv_row", "gemv_col"):
+        # a stream over the matrix: bound by HBM bandwidth
+        hbm, src = measured_hbm_gbs()
+        gbs = 4 * (M * K + K * N + M * N) / (ms_step * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                "frac": gbs / hbm,
+                "traffic": recorded_traffic(kernel, w["name"]),
+                "kernel": kernel,
+                "peak_basis": "HBM copy bandwidth %.1f GB/s (%s, "
+                              "MEASURED_PEAKS.json); algorithmic bytes "
+                              "4(MK + KN + MN)" % (hbm, src)}
     else:
         roof = {"bound": "alu", "achieved": tflops, "peak": ffma_peak,
                 "unit": "TFLOP/s", "frac": tflops / ffma_peak,
@@ -463,8 +511,9 @@ def run_gpu(args, w):
             "arithmetic": ("3xTF32 tensor-core products (hi/lo split), fp32 "
                            "accumulation" if plan.startswith("tf32x3") else
                            "fp32 fused multiply-add on CUDA cores"),
-            "l2": "flushed before every step (256 MiB device memset, "
-                  "outside the timed events)",
+            "l2": "flushed before every step (a 256 MiB device write, then "
+                  "a 256 MiB read so no dirty lines remain; outside the timed "
+                  "events)",
             "parallelism": "replicas" if world > 1 else "single GPU"}),
         "roofline": roof,
         "pct_of_ffma_peak": 100.0 * tflops / ffma_peak,
