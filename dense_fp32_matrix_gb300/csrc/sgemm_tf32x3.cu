@@ -470,7 +470,6 @@ constexpr int PM = 256, PN = 256;
 constexpr int P_THREADS = 448;
 constexpr int P_PREFETCH = 3;                        // k-slices ahead into L2
 constexpr int P_CONV_WARPS = 8;
-constexpr int P_CONV_THREADS = 32 * P_CONV_WARPS;
 constexpr int P_ACC_COLS = 256;                      // one accumulator
 constexpr int P_TMEM_COLS = 2 * P_ACC_COLS;           // all of it
 constexpr int P_ALO_COL = P_ACC_COLS;                 // A_lo stages (K-major A)
@@ -972,7 +971,6 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // tensor-memory lanes of this warp
-    const int row = 32 * quarter + lane;  // row within the block's half
     const uint32_t acce_leader = cluster_map(acce0, 0);
     float4* ws4 = reinterpret_cast<float4*>(p.ws);
     // Stream-K tiles whose pieces this warp sums (a cluster's share of
