@@ -617,28 +617,36 @@ struct Unit {
   int sk;      // stream-K tile index when the unit is a partial piece, else -1
 };
 
-// Unit u of cluster c; false past the cluster's last unit.
+// Unit u of cluster c; false past the cluster's last unit. A cluster first
+// works through its stream-K share (at most two partial segments), then its
+// whole tiles: the fix-ups of the split tiles then run while the clusters
+// multiply their whole tiles, instead of after them at the end of the launch.
 __device__ __forceinline__ bool unit_of(int c, int u, const PairParams& p,
                                         Unit& w) {
   const int dp_units = c < p.dp_tiles ? (p.dp_tiles - c + p.G - 1) / p.G : 0;
-  if (u < dp_units) {
-    w.tile = c + u * p.G;
-    w.kb = 0;
-    w.ke = p.T;
-    w.sk = -1;
+  int sk_units = 0;
+  long long b = 0, e = 0;
+  if (p.sk_tiles > 0) {
+    b = sk_begin(c, p);
+    e = sk_begin(c + 1, p);
+    if (b < e) sk_units = int((e - 1) / p.T - b / p.T + 1);
+  }
+  if (u < sk_units) {
+    const long long x = u == 0 ? b : (b / p.T + u) * p.T;
+    const int tau = int(x / p.T);
+    const long long x0 = (long long)tau * p.T;
+    w.tile = p.dp_tiles + tau;
+    w.kb = int(x - x0);
+    w.ke = int(e - x0 < p.T ? e - x0 : p.T);
+    w.sk = (w.kb == 0 && w.ke == p.T) ? -1 : tau;
     return true;
   }
-  if (p.sk_tiles == 0) return false;
-  const long long b = sk_begin(c, p), e = sk_begin(c + 1, p);
-  const int v = u - dp_units;
-  const long long x = v == 0 ? b : (b / p.T + v) * p.T;
-  if (x >= e) return false;
-  const int tau = int(x / p.T);
-  const long long x0 = (long long)tau * p.T;
-  w.tile = p.dp_tiles + tau;
-  w.kb = int(x - x0);
-  w.ke = int(e - x0 < p.T ? e - x0 : p.T);
-  w.sk = (w.kb == 0 && w.ke == p.T) ? -1 : tau;
+  u -= sk_units;
+  if (u >= dp_units) return false;
+  w.tile = c + u * p.G;
+  w.kb = 0;
+  w.ke = p.T;
+  w.sk = -1;
   return true;
 }
 
@@ -741,7 +749,84 @@ __device__ __forceinline__ void store_c_tma(uint32_t acc, uint8_t* stg,
   }
 }
 
-template <int OA, int OB>
+// Piece j of stream-K tile `sk` for one block and lane quarter: the
+// contributors are clusters c_first .. c_first + pieces - 1 in k order, and
+// only the first one's share can start before the tile, so only its piece
+// can sit in its second workspace slot.
+__device__ __forceinline__ const float4* sk_piece(const float4* ws4, int sk,
+                                                  int j, uint32_t rank,
+                                                  int quarter,
+                                                  const PairParams& p) {
+  const long long x0 = (long long)sk * p.T;
+  const int c_first = sk_owner(x0, p);
+  const int s_first = sk_begin(c_first, p) >= x0 ? 0 : 1;
+  return ws4 + ((long long)((c_first + j) * 2 + (j == 0 ? s_first : 0)) * 2 +
+                rank) * (P_PIECE_FLOATS / 4) + quarter * 8 * 256;
+}
+
+// Stream-K fix-up of one lane quarter of a tile while the block still has a
+// whole tile to multiply: the stage ring is busy, so the pieces are read
+// straight from L2 (a piece's column block is 4 KiB, warp-major: element
+// (e, lane) at e * 32 + lane, so each load is 512 coalesced bytes) and each
+// lane writes its row's sums straight to C (its 32 columns of a block are
+// 128 contiguous bytes). The pieces are added in k order, exactly as in the
+// end-of-kernel fix-up, so the result does not depend on which of the two
+// runs.
+__device__ __forceinline__ void fixup_direct(const float4* ws4, int tile,
+                                             uint32_t rank, int quarter,
+                                             int lane, const PairParams& p) {
+  int item, pm, pn;
+  pair_tile(tile, p, item, pm, pn);
+  const int sk = tile - p.dp_tiles;
+  const long long x0 = (long long)sk * p.T;
+  const int pieces = sk_owner(x0 + p.T - 1, p) - sk_owner(x0, p) + 1;
+  const int n0 = pn * PN;
+  const int r0q = pm * PM + 128 * int(rank) + 32 * quarter;
+  if (r0q + lane >= p.M) return;
+  float* crow = p.C + item * p.bt.stride_c + (long long)(r0q + lane) * p.ldc +
+                n0;
+  const int cols_in = p.N - n0 < PN ? p.N - n0 : PN;
+#pragma unroll 1
+  for (int cb = 0; cb < PN / 32; ++cb) {
+    float4 acc[8];
+#pragma unroll 1
+    for (int j = 0; j < pieces; ++j) {
+      const float4* src =
+          sk_piece(ws4, sk, j, rank, quarter, p) + cb * 256 + lane;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float4 x = __ldcg(src + e * 32);
+        if (j == 0) {
+          acc[e] = x;
+        } else {
+          acc[e].x += x.x;
+          acc[e].y += x.y;
+          acc[e].z += x.z;
+          acc[e].w += x.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int col = 32 * cb + 4 * e;
+      float* c = crow + col;
+      if (p.vec_store && col + 3 < cols_in) {
+        *reinterpret_cast<float4*>(c) = epi4(acc[e], c, p.sc);
+      } else {
+        const float v[4] = {acc[e].x, acc[e].y, acc[e].z, acc[e].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (col + i < cols_in) c[i] = epi1(v[i], c + i, p.sc);
+      }
+    }
+  }
+}
+
+// kEarlyFix: schedules with whole tiles after the stream-K shares sum a
+// split tile's pieces as soon as they are in (under the next MMAs). It is
+// a template switch so that schedules without whole tiles (all split, or
+// none split) keep the code of the end-of-kernel fix-up alone.
+template <int OA, int OB, bool kEarlyFix>
 __global__ void __launch_bounds__(P_THREADS, 1)
 k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
               const __grid_constant__ CUtensorMap tmB,
@@ -1048,8 +1133,18 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       const int pieces = sk_owner(x0 + p.T - 1, p) - c_first + 1;
       if (arrived != pieces - 1) continue;
       __threadfence();
-      // the last piece in: sum the pieces once this warp's own units are
-      // done (then the stage buffers are free for a deep copy pipeline)
+      // The last piece is in. If this cluster's stream-K share ends inside
+      // this tile and whole tiles follow (they come after the share), the
+      // stage ring stays busy for a whole tile: sum the pieces now, under
+      // those MMAs. Otherwise (only partial segments left) defer it until
+      // this warp's units are done, when the ring is free for a deep copy
+      // pipeline.
+      if (kEarlyFix && w.ke < p.T && cl < p.dp_tiles) {
+        fixup_direct(ws4, w.tile, rank, quarter, lane, p);
+        __syncwarp();
+        if (lane == 0) p.counters[(w.sk * 2 + int(rank)) * 4 + quarter] = 0;
+        continue;
+      }
       if (nfix < kMaxFix) fix_tile[nfix++] = w.tile;
 
     }
@@ -1201,7 +1296,11 @@ cudaError_t set_smem_attrs() {
       k_tf32x3<OA, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       int(X_SMEM));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_tf32x3_pair<OA, OB>,
+  const cudaError_t e2 = cudaFuncSetAttribute(
+      k_tf32x3_pair<OA, OB, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      int(P_SMEM));
+  if (e2 != cudaSuccess) return e2;
+  return cudaFuncSetAttribute(k_tf32x3_pair<OA, OB, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(P_SMEM));
 }
@@ -1224,7 +1323,7 @@ cudaError_t tf32x3_init(int* pair_clusters) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, k_tf32x3_pair<0, 0>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, k_tf32x3_pair<0, 0, false>, &cfg);
   if (e != cudaSuccess) return e;
   *pair_clusters = n;
   return n > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
@@ -1314,15 +1413,24 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  switch (g.op_a * 2 + g.op_b) {
-    case 0: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0>, tmA, tmB,
-                                     mapC, p);
-    case 1: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1>, tmA, tmB,
-                                     mapC, p);
-    case 2: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0>, tmA, tmB,
-                                     mapC, p);
-    default: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1>, tmA, tmB,
-                                     mapC, p);
+  const bool early = pl.dp_tiles > 0 && pl.sk_tiles > 0;
+  switch (g.op_a * 4 + g.op_b * 2 + (early ? 1 : 0)) {
+    case 0: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0, false>, tmA,
+                                      tmB, mapC, p);
+    case 1: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0, true>, tmA,
+                                      tmB, mapC, p);
+    case 2: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1, false>, tmA,
+                                      tmB, mapC, p);
+    case 3: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1, true>, tmA,
+                                      tmB, mapC, p);
+    case 4: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0, false>, tmA,
+                                      tmB, mapC, p);
+    case 5: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0, true>, tmA,
+                                      tmB, mapC, p);
+    case 6: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1, false>, tmA,
+                                      tmB, mapC, p);
+    default: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1, true>, tmA,
+                                       tmB, mapC, p);
   }
 }
 

@@ -203,3 +203,18 @@ def test_pair_matches_masked_high_part_bitwise(mnk, kind):
     C2 = dfm.matmul(A, B, path=PAIR)
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
+
+
+# Schedules with whole tiles after the stream-K shares (2300 x 2900 x 1900:
+# 108 tiles, 76 whole + 32 split on 76 clusters) sum a split tile's pieces
+# as soon as the last one is in and write C straight from registers: alpha,
+# beta, and rows that are not 16-byte aligned (pad 1) all go through it.
+@pytest.mark.parametrize("pad", [4, 1])
+@pytest.mark.parametrize("ops", [("N", "N"), ("T", "T")], ids="".join)
+@pytest.mark.parametrize("kind,alpha,beta", [("integers", 0.5, 2.0),
+                                             ("uniform", 0.75, -1.5),
+                                             ("uniform", 1.0, 0.0)])
+def test_pair_early_fixup_epilogue(pad, ops, kind, alpha, beta):
+    from test_ex_gpu import run_ex
+    run_ex(*ops, 2300, 2900, 1900, alpha, beta, kind=kind, seed=7, path=PAIR,
+           pad=pad)
