@@ -473,6 +473,7 @@ constexpr int P_CONV_WARPS = 8;
 constexpr int P_ACC_COLS = 256;                      // one accumulator
 constexpr int P_TMEM_COLS = 2 * P_ACC_COLS;           // all of it
 constexpr int P_ALO_COL = P_ACC_COLS;                 // A_lo stages (K-major A)
+constexpr int P_PARK_COL = P_ALO_COL + 128;           // parked half accumulator
 static_assert(P_ALO_COL + XSTAGES * XK <= P_TMEM_COLS, "A_lo stages fit");
 constexpr int P_EPI_WARP0 = 2 + P_CONV_WARPS;
 constexpr int P_EPI_ARRIVALS = 2 * 4;                // 4 warps x 2 blocks
@@ -552,6 +553,30 @@ __device__ __forceinline__ void a_lo_to_tmem(const uint8_t* A, uint32_t col,
 // the landed tile is the high part, all threads write the low part. One
 // MN-major operand: two warps per box, one per 16-k half. Both MN-major:
 // one box per warp.
+// Copies accumulator columns 128 .. 255 of this warp's lanes to the
+// tensor-memory columns park .. park + 127 (not used by the MMAs), so that
+// the accumulator can be handed back after only its lower half has gone out
+// through the staging boxes; the parked half is stored under the next
+// tile's MMAs. Tensor-memory loads take tens of cycles, a bulk store's
+// staging box about a thousand.
+__device__ __forceinline__ void park_upper_half(uint32_t acc, uint32_t park) {
+#pragma unroll 1
+  for (int cb = 4; cb < 8; ++cb) {
+    uint32_t v[32];
+    tc::tmem_ld_32x32b_x32(acc + 32 * cb, v);
+    tc::tmem_ld_wait();
+    uint32_t lo[16], hi[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      lo[i] = v[i];
+      hi[i] = v[16 + i];
+    }
+    tc::tmem_st_32x32b_x16(park + 32 * (cb - 4), lo);
+    tc::tmem_st_32x32b_x16(park + 32 * (cb - 4) + 16, hi);
+  }
+  tc::tmem_st_wait();
+}
+
 template <int OA, int OB>
 __device__ __forceinline__ void split_stage_pair(uint8_t* A, uint8_t* Alo,
                                                  uint8_t* B, uint8_t* Blo,
@@ -721,12 +746,13 @@ __device__ __forceinline__ void store_c_staged(uint32_t acc, uint8_t* box,
 // 32 x 32 box with the 128-byte swizzle (16-byte chunk c of row r at
 // c ^ (r & 7): conflict-free), then lane 0 stores the box. A box is reused
 // once the store issued from it two boxes earlier has read it.
+// Column blocks cb0 .. cb1 - 1 of 32 (accumulator column acc + 32 cb).
 __device__ __forceinline__ void store_c_tma(uint32_t acc, uint8_t* stg,
                                             const CUtensorMap* tmC, int lane,
                                             int x0, int y0, int z,
-                                            float alpha) {
+                                            float alpha, int cb0, int cb1) {
 #pragma unroll 1
-  for (int cb = 0; cb < PN / 32; ++cb) {
+  for (int cb = cb0; cb < cb1; ++cb) {
     uint32_t v[32];
     tc::tmem_ld_32x32b_x32(acc + 32 * cb, v);
     tc::tmem_ld_wait();
@@ -842,6 +868,9 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
   constexpr int kStages = kLoTmem ? 4 : 3;
   static_assert(kStages * kStageBytes <= XSTAGES * X_STAGE, "ring fits");
   static_assert(P_ALO_COL + kStages * XK <= P_TMEM_COLS, "A_lo fits");
+  static_assert(!kLoTmem || (P_ALO_COL + kStages * XK <= P_PARK_COL &&
+                             P_PARK_COL + 128 <= P_TMEM_COLS),
+                "the parked half is clear of A_lo");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -1083,8 +1112,17 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
       const int cols_in = p.N - n0 < PN ? p.N - n0 : PN;
       uint8_t* stg = stg0 + (warp - P_EPI_WARP0) * 2 * P_STG_BOX;
       int slot = 0;
-      if (w.sk < 0 && p.tma_c) {
-        store_c_tma(acc, stg, &tmC, lane, n0, r0q, item, p.sc.alpha);
+      // one accumulator (A_lo holds the rest of tensor memory except the
+      // last 128 columns): park its upper half there, hand it back sooner
+      const uint32_t park = tmem + uint32_t(P_PARK_COL) +
+                            (uint32_t(32 * quarter) << 16);
+      const bool parked = kLoTmem && w.sk < 0 && p.tma_c;
+      if (parked) {
+        park_upper_half(acc, park);
+        store_c_tma(acc, stg, &tmC, lane, n0, r0q, item, p.sc.alpha, 0, 4);
+      } else if (w.sk < 0 && p.tma_c) {
+        store_c_tma(acc, stg, &tmC, lane, n0, r0q, item, p.sc.alpha, 0,
+                    PN / 32);
       } else if (w.sk < 0) {
         store_c_staged(acc, stg, cq, p.ldc, rows_in, cols_in, lane, p.sc);
       } else {
@@ -1120,6 +1158,9 @@ k_tf32x3_pair(const __grid_constant__ CUtensorMap tmA,
         else
           mbar_arrive_cluster(acce_leader + 8 * b);
       }
+      if (parked)  // column block cb of the parked half at park + 32 (cb - 4)
+        store_c_tma(park - 128, stg, &tmC, lane, n0, r0q, item, p.sc.alpha, 4,
+                    PN / 32);
       if (w.sk < 0) continue;
       // ------------------------------------------------ stream-K fixup
       __threadfence();
