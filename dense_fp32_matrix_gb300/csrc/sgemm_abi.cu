@@ -369,10 +369,14 @@ int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
   Workspace* w = nullptr;
   const int wrc = ensure_workspace(st, s, pl.ws_floats, pl.counters, &w);
   if (wrc != SGEMM_OK) return wrc;
-  // C by bulk tensor stores when it is not read (beta == 0) and aligned
+  // C by bulk tensor stores when it is not read (beta == 0) and aligned.
+  // Rows must also end on a 16-byte boundary (N a multiple of 4): a bulk
+  // tensor store writes the last 16-byte chunk of a row whole, so with
+  // N % 4 != 0 it would write up to 3 floats past column N - 1 (into the
+  // pitch padding, or past the end of C on the last row).
   CUtensorMap tmC;
   const bool c_ok =
-      g.sc.beta == 0.f &&
+      g.sc.beta == 0.f && g.N % 4 == 0 &&
       tma_operand_ok(reinterpret_cast<uint64_t>(g.C), g.ldc) &&
       (g.batch <= 1 || g.stride_c % 4 == 0) &&
       encode_3d(&tmC, g.C, g.N, g.M, g.ldc, g.batch, g.stride_c, 32, 32,

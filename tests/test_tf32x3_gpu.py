@@ -218,3 +218,15 @@ def test_pair_early_fixup_epilogue(pad, ops, kind, alpha, beta):
     from test_ex_gpu import run_ex
     run_ex(*ops, 2300, 2900, 1900, alpha, beta, kind=kind, seed=7, path=PAIR,
            pad=pad)
+
+
+# C with rows that do not end on a 16-byte boundary (N % 4 != 0) inside a
+# 16-byte-aligned pitch: a bulk tensor store writes whole 16-byte chunks, so
+# these must take the staged row stores; the pitch padding stays untouched
+# (whole tiles, split tiles, every tile split).
+@pytest.mark.parametrize("mnk,ldc", [((1893, 1777, 426), 1780),
+                                     ((2300, 2901, 1900), 2904),
+                                     ((1000, 1001, 1000), 1004),
+                                     ((300, 203, 64), 208)], ids=str)
+def test_pair_never_writes_past_row_end(mnk, ldc):
+    run_case(*mnk, kind="integers", seed=5, ldc=ldc, path=PAIR)
