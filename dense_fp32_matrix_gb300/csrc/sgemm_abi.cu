@@ -695,9 +695,11 @@ int run_batched(const Call& c, int64_t stride_a, int64_t stride_b,
     path = pair_work(c.M, c.N, c.K, batch) >= kTf32PairMinWork
                ? SGEMM_PATH_TF32X3_PAIR
                : SGEMM_PATH_TF32X3;
-  if (reads_ab(c) &&
+  // One launch for the batch on the tensor path; a forced tensor path on
+  // operands it cannot map whole (misaligned rows or strides) runs item by
+  // item below, where each item is repacked like a single call.
+  if (reads_ab(c) && tensor_ok &&
       (path == SGEMM_PATH_TF32X3 || path == SGEMM_PATH_TF32X3_PAIR)) {
-    if (!tensor_ok) return SGEMM_ERR_PATH;
     DeviceState* st = nullptr;
     rc = device_state(&st);
     if (rc != SGEMM_OK) return rc;

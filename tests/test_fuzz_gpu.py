@@ -61,3 +61,77 @@ def test_random_shapes(case):
         if path == "tiled_tma" and e.status == dfm.STATUS["SGEMM_ERR_PATH"]:
             pytest.skip("tiled_tma refuses this layout")
         raise
+
+
+def _batch_cases(n=20, seed=77):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        M, N, K = (int(round(np.exp(rng.uniform(0.0, np.log(hi)))))
+                   for hi in (700, 700, 600))
+        batch = int(rng.integers(1, 6))
+        if M * N * K * batch > 6e8:
+            continue
+        ops = ("N", "T")[rng.integers(2)], ("N", "T")[rng.integers(2)]
+        kind = ("uniform", "integers")[rng.integers(2)]
+        alpha, beta = [(1.0, 0.0), (0.5, 2.0)][rng.integers(2)]
+        shared = int(rng.integers(3))  # 0 none, 1 A shared, 2 B shared
+        side = bool(rng.integers(2))
+        path = ("auto", "tf32x3_pair", "tiled_ldg")[rng.integers(3)]
+        out.append((M, N, K, batch, ops, kind, alpha, beta, shared, side,
+                    path, int(rng.integers(1 << 20))))
+    return out
+
+
+BATCH_CASES = _batch_cases()
+
+
+@pytest.mark.parametrize(
+    "case", BATCH_CASES,
+    ids=["%dx%dx%dx%d-%s%s-%s-%g-%g-s%d-%s-%s" % (
+        c[0], c[1], c[2], c[3], *c[4], c[5], c[6], c[7], c[8],
+        "side" if c[9] else "stacked", c[10]) for c in BATCH_CASES])
+def test_random_batches(case):
+    from test_batched_gpu import run_batch
+    M, N, K, batch, ops, kind, alpha, beta, shared, side, path, seed = case
+    run_batch(ops, M, N, K, batch, alpha=alpha, beta=beta, kind=kind,
+              seed=seed, path=path, shared_a=shared == 1,
+              shared_b=shared == 2, side_by_side=side)
+
+
+def _layout_cases(n=24, seed=4242):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        shape = rng.integers(4)
+        M, N, K = (int(round(np.exp(rng.uniform(0.0, np.log(hi)))))
+                   for hi in (3000, 3000, 3000))
+        if shape == 0:
+            M = 1
+        elif shape == 1:
+            N = 1
+        if M * N * K > 3e9:
+            continue
+        pads = [int(rng.integers(0, 5)) for _ in range(3)]
+        offs = tuple(int(rng.integers(0, 4)) for _ in range(3))
+        out.append((M, N, K, pads, offs, ("uniform", "integers")[
+            rng.integers(2)], int(rng.integers(1 << 20))))
+    return out
+
+
+LAYOUT_CASES = _layout_cases()
+
+
+@pytest.mark.parametrize(
+    "case", LAYOUT_CASES,
+    ids=["%dx%dx%d-pad%s-off%s-%s" % (c[0], c[1], c[2], "".join(map(str, c[3])),
+                                      "".join(map(str, c[4])), c[5])
+         for c in LAYOUT_CASES])
+def test_random_layouts(case):
+    # sgemm (default dispatch) on pitched and misaligned operands: the
+    # vector kernels, the repack before the tensor path, and the any-layout
+    # tile kernel all get picked somewhere in here.
+    from gpu_util import run_case
+    M, N, K, pads, offs, kind, seed = case
+    run_case(M, N, K, kind=kind, seed=seed, lda=max(K, 1) + pads[0],
+             ldb=max(N, 1) + pads[1], ldc=max(N, 1) + pads[2], offsets=offs)
