@@ -135,3 +135,47 @@ def test_random_layouts(case):
     M, N, K, pads, offs, kind, seed = case
     run_case(M, N, K, kind=kind, seed=seed, lda=max(K, 1) + pads[0],
              ldb=max(N, 1) + pads[1], ldc=max(N, 1) + pads[2], offsets=offs)
+
+
+def _host_cases(n=12, seed=99):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        M, N, K = (int(round(np.exp(rng.uniform(0.0, np.log(hi)))))
+                   for hi in (3000, 2500, 2000))
+        if len(out) < 4:  # large enough for the row-block pipeline
+            M, N, K = (int(rng.integers(512, 3000)),
+                       int(rng.integers(600, 2500)),
+                       int(rng.integers(1200, 2000)))
+        if M * N * K > 8e9:
+            continue
+        pads = [int(rng.integers(0, 5)) for _ in range(3)]
+        out.append((M, N, K, pads, ("uniform", "integers")[rng.integers(2)],
+                    int(rng.integers(1 << 20))))
+    return out
+
+
+HOST_CASES = _host_cases()
+
+
+@pytest.mark.parametrize(
+    "case", HOST_CASES,
+    ids=["%dx%dx%d-pad%s-%s" % (c[0], c[1], c[2], "".join(map(str, c[3])),
+                                c[4]) for c in HOST_CASES])
+def test_random_host_products(case):
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    import matgen
+    import oracle
+    from gpu_util import compare
+    from test_host_pipeline_gpu import host_product
+    M, N, K, pads, kind, seed = case
+    A = matgen.KINDS[kind](seed, matgen.MATRIX_A, M, K)
+    B = matgen.KINDS[kind](seed, matgen.MATRIX_B, K, N)
+    hC, _ = host_product(A, B, M, N, K, *pads)
+    torch.cuda.synchronize()
+    assert dfm.sgemm_watchdog_status() == (0, 0)
+    if pads[2]:
+        assert torch.isnan(hC[:, N:]).all()      # pitch padding untouched
+    ref, S = oracle.gemm(A, B)
+    compare(kind, hC[:, :N].numpy(), ref, S, "sgemm_host %dx%dx%d" % (M, N, K))
