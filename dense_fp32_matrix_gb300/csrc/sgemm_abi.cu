@@ -752,7 +752,13 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
   if (K == 0)
     return to_status(cudaMemset2DAsync(C, size_t(ldc) * 4, 0, size_t(N) * 4,
                                        size_t(M), s));
-  const int path = plan_path(M, N, K, lda, ldb, a, b);
+  int path = plan_path(M, N, K, lda, ldb, a, b);
+  // The tensor paths take misaligned operands through a repacked copy,
+  // which needs device memory: here such operands go to the any-layout
+  // tile kernel instead.
+  if ((path == SGEMM_PATH_TF32X3 || path == SGEMM_PATH_TF32X3_PAIR) &&
+      !(tma_operand_ok(a, lda) && tma_operand_ok(b, ldb)))
+    path = SGEMM_PATH_TILED_LDG;
   const GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc};
   switch (path) {
     case SGEMM_PATH_TILED_TMA: {

@@ -253,7 +253,9 @@ int sgemm_host(int64_t M, int64_t N, int64_t K, const float* hA, int64_t lda,
  * the library holds until the process exits. Limits: at most 16384 output
  * tiles of 128 x 128 (e.g. M = N = 16384); larger M x N returns
  * SGEMM_ERR_TOO_LARGE before any work is enqueued. The stream-K grid is
- * capped at 160 blocks.
+ * capped at 160 blocks. Operands whose base or row stride is not 16-byte
+ * aligned take the any-layout CUDA-core tile kernel (sgemm would repack
+ * them into allocated memory for the tensor path).
  *
  * The first call on a device fetches the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call

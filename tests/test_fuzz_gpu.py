@@ -179,3 +179,48 @@ def test_random_host_products(case):
         assert torch.isnan(hC[:, N:]).all()      # pitch padding untouched
     ref, S = oracle.gemm(A, B)
     compare(kind, hC[:, :N].numpy(), ref, S, "sgemm_host %dx%dx%d" % (M, N, K))
+
+
+def _noalloc_cases(n=12, seed=5150):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        M, N, K = (int(round(np.exp(rng.uniform(0.0, np.log(hi)))))
+                   for hi in (3000, 3000, 2500))
+        if M * N * K > 6e9:
+            continue
+        out.append((M, N, K, ("auto", "ffma")[rng.integers(2)],
+                    ("uniform", "integers")[rng.integers(2)],
+                    int(rng.integers(1 << 20))))
+    return out
+
+
+NOALLOC_CASES = _noalloc_cases()
+
+
+@pytest.mark.parametrize(
+    "case", NOALLOC_CASES,
+    ids=["%dx%dx%d-%s-%s" % c[:5] for c in NOALLOC_CASES])
+def test_random_noalloc(case):
+    # the fixed-scratch entry point, in both math modes, against the oracle
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    import matgen
+    import oracle
+    from gpu_util import compare
+    M, N, K, mode, kind, seed = case
+    A_h = matgen.KINDS[kind](seed, matgen.MATRIX_A, M, K)
+    B_h = matgen.KINDS[kind](seed, matgen.MATRIX_B, K, N)
+    A = torch.from_numpy(A_h).cuda()
+    B = torch.from_numpy(B_h).cuda()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    prev = dfm.sgemm_set_math_mode(mode)
+    try:
+        dfm.sgemm_noalloc(M, N, K, A, max(K, 1), B, max(N, 1), C, max(N, 1))
+        torch.cuda.synchronize()
+    finally:
+        dfm.sgemm_set_math_mode(prev)
+    assert dfm.sgemm_watchdog_status() == (0, 0)
+    ref, S = oracle.gemm(A_h, B_h)
+    compare(kind, C.cpu().numpy(), ref, S, "sgemm_noalloc %dx%dx%d %s" % (
+        M, N, K, mode))
