@@ -224,3 +224,48 @@ def test_random_noalloc(case):
     ref, S = oracle.gemm(A_h, B_h)
     compare(kind, C.cpu().numpy(), ref, S, "sgemm_noalloc %dx%dx%d %s" % (
         M, N, K, mode))
+
+
+def _mode_cases(n=16, seed=31337):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        if len(out) < 6:   # long k, few outputs: every tile split
+            M, N = (int(round(np.exp(rng.uniform(0.0, np.log(700)))))
+                    for _ in range(2))
+            K = int(rng.integers(8000, 30000))
+        else:
+            M, N, K = (int(round(np.exp(rng.uniform(0.0, np.log(hi)))))
+                       for hi in (2500, 2500, 2500))
+        if M * N * K > 4e9:
+            continue
+        ops = ("N", "T")[rng.integers(2)], ("N", "T")[rng.integers(2)]
+        kind = ("uniform", "integers")[rng.integers(2)]
+        if kind == "integers":
+            alpha, beta = [(1.0, 0.0), (0.5, 2.0)][rng.integers(2)]
+        else:
+            alpha, beta = [(1.0, 0.0), (0.75, -1.5)][rng.integers(2)]
+        out.append((M, N, K, ops, kind, alpha, beta,
+                    ("auto", "ffma")[rng.integers(2)],
+                    int(rng.integers(0, 6)), int(rng.integers(1 << 20))))
+    return out
+
+
+MODE_CASES = _mode_cases()
+
+
+@pytest.mark.parametrize(
+    "case", MODE_CASES,
+    ids=["%dx%dx%d-%s%s-%s-%g-%g-%s-p%d" % (c[0], c[1], c[2], *c[3], c[4],
+                                           c[5], c[6], c[7], c[8])
+         for c in MODE_CASES])
+def test_random_math_modes(case):
+    # default dispatch in both math modes (the CUDA-core kernels and the
+    # vector kernels in "ffma"), including long-k products
+    import dense_fp32_matrix_gb300 as dfm
+    M, N, K, ops, kind, alpha, beta, mode, pad, seed = case
+    prev = dfm.sgemm_set_math_mode(mode)
+    try:
+        run_ex(*ops, M, N, K, alpha, beta, kind=kind, seed=seed, pad=pad)
+    finally:
+        dfm.sgemm_set_math_mode(prev)
