@@ -126,8 +126,16 @@ cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
 // tf32x3_init also reports how many 2-block clusters of the pair kernel fit
 // on the device at once.
 cudaError_t tf32x3_init(int* pair_clusters);
+// Split-k for products whose tiles fill under half of the SMs: splits > 1
+// multiplies k ranges into `part` (tf32x3_split_floats floats) and adds them
+// in order in a second kernel; splits == 1 (or part == nullptr) stores C
+// directly.
+int plan_tf32x3_splits(int64_t M, int64_t N, int64_t K, int64_t batch,
+                       int sms);
+size_t tf32x3_split_floats(int64_t M, int64_t N, int64_t batch, int splits);
 cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
-                          const CUtensorMap& tmB, int* status, cudaStream_t s);
+                          const CUtensorMap& tmB, int* status, cudaStream_t s,
+                          int splits = 1, float* part = nullptr);
 
 // 2-SM variant: 256 x 256 tiles, persistent clusters of 2 blocks with a
 // stream-K tail (same maps: each block loads A boxes {32, 128} and B boxes

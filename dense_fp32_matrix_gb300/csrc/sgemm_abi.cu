@@ -30,9 +30,23 @@ constexpr int64_t kTf32RepackMinMacs = int64_t(1) << 24;
 // one 1-SM block per 128 x 128 tile (measured: 1024^3 and every long-K
 // shape of few tiles go to pairs, 512^3 stays on single blocks).
 constexpr int64_t kTf32PairMinWork = 256;
+// Below this many 128 x 128 tiles (half of GB300's 152 SMs) single blocks
+// split k over the idle SMs; with short k (up to this many k-slices) that
+// beats the pairs' stream-K split (1024^3: 29 vs 35 us), with longer k the
+// pairs win (1024 x 1024 x 4096: 59 vs 78 us).
+constexpr int64_t kSplitMaxTiles = 76;
+constexpr int64_t kSplitMaxSlices = 32;
 
 int64_t pair_work(int64_t M, int64_t N, int64_t K, int64_t batch) {
   return batch * ((M + 255) / 256) * ((N + 255) / 256) * ((K + 31) / 32);
+}
+
+// The tensor path's kernel: 2-SM pairs, or single blocks (split-k when the
+// tiles are few).
+bool use_pair(int64_t M, int64_t N, int64_t K, int64_t batch) {
+  if (pair_work(M, N, K, batch) < kTf32PairMinWork) return false;
+  const int64_t tiles = batch * ((M + 127) / 128) * ((N + 127) / 128);
+  return !(tiles <= kSplitMaxTiles && (K + 31) / 32 <= kSplitMaxSlices);
 }
 // Largest M, N or K the int-indexed kernels accept (tile rounding included).
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1024;
@@ -359,11 +373,23 @@ int encode_tf32x3(const GemmArgs& g, CUtensorMap* tmA, CUtensorMap* tmB) {
 
 // (st.ws_mu held: the pair kernel uses the stream's workspace.)
 int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
-               bool pair) {
+               bool pair, bool may_alloc = true) {
   CUtensorMap tmA, tmB;
   const int rc = encode_tf32x3(g, &tmA, &tmB);
   if (rc != SGEMM_OK) return rc;
-  if (!pair) return to_status(launch_tf32x3(g, tmA, tmB, st.status, s));
+  if (!pair) {
+    // few tiles: split k over the idle SMs (the pieces need workspace)
+    const int splits =
+        may_alloc ? plan_tf32x3_splits(g.M, g.N, g.K, g.batch, st.sms) : 1;
+    if (splits == 1)
+      return to_status(launch_tf32x3(g, tmA, tmB, st.status, s));
+    Workspace* w = nullptr;
+    const int wrc = ensure_workspace(
+        st, s, tf32x3_split_floats(g.M, g.N, g.batch, splits), 0, &w);
+    if (wrc != SGEMM_OK) return wrc;
+    return to_status(
+        launch_tf32x3(g, tmA, tmB, st.status, s, splits, w->ws));
+  }
   const PairPlan pl =
       plan_pair(g.M, g.N, g.K, st.pair_clusters, true, g.batch);
   Workspace* w = nullptr;
@@ -455,9 +481,8 @@ int plan_call(const Call& c) {
       double(c.M) * double(c.N) * double(c.K) >= double(kTf32RepackMinMacs);
   if ((aligned || repack_pays) &&
       g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO) {
-    return pair_work(c.M, c.N, c.K, 1) >= kTf32PairMinWork
-               ? SGEMM_PATH_TF32X3_PAIR
-                                           : SGEMM_PATH_TF32X3;
+    return use_pair(c.M, c.N, c.K, 1) ? SGEMM_PATH_TF32X3_PAIR
+                                      : SGEMM_PATH_TF32X3;
   }
   // CUDA-core tile kernels take row-major operands; a transposed one is
   // first copied row-major (dense, ld = its width) into the workspace.
@@ -692,9 +717,8 @@ int run_batched(const Call& c, int64_t stride_a, int64_t stride_b,
   if (path == SGEMM_PATH_AUTO && tensor_ok &&
       g_math_mode.load(std::memory_order_relaxed) == SGEMM_MATH_AUTO &&
       c.M > 1 && c.N > 1)
-    path = pair_work(c.M, c.N, c.K, batch) >= kTf32PairMinWork
-               ? SGEMM_PATH_TF32X3_PAIR
-               : SGEMM_PATH_TF32X3;
+    path = use_pair(c.M, c.N, c.K, batch) ? SGEMM_PATH_TF32X3_PAIR
+                                          : SGEMM_PATH_TF32X3;
   // One launch for the batch on the tensor path; a forced tensor path on
   // operands it cannot map whole (misaligned rows or strides) runs item by
   // item below, where each item is repacked like a single call.
@@ -779,7 +803,7 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
     case SGEMM_PATH_TF32X3:
-      return run_tf32x3(g, *st, s, false);
+      return run_tf32x3(g, *st, s, false, false);
     case SGEMM_PATH_TF32X3_PAIR: {
       CUtensorMap tmA, tmB;
       rc = encode_tf32x3(g, &tmA, &tmB);

@@ -269,12 +269,19 @@ __device__ __forceinline__ void tile_of(int tile, int tiles_m, int tiles_n,
   pn = in_group / rows;
 }
 
+// Split-k (splits > 1, blockIdx.y = split): the block multiplies k-slices
+// [split T / splits, (split + 1) T / splits) of its tile and writes the raw
+// accumulator to `part`, block-major (tile x splits, 4096 float4 each,
+// warp-major inside: float4 ((q * 4 + cb) * 8 + e) * 32 + lane holds row
+// 32 q + lane, columns 32 cb + 4 e .. + 3); k_splitk_reduce adds the splits
+// in order and applies the epilogue.
 template <int OA, int OB>
 __global__ void __launch_bounds__(X_THREADS, 1)
 k_tf32x3(const __grid_constant__ CUtensorMap tmA,
          const __grid_constant__ CUtensorMap tmB, float* __restrict__ C, int M,
          int N, int K, long long ldc, int tiles_m, int tiles_n, int vec_store,
-         Scale sc, Batch bt, int* status) {
+         Scale sc, Batch bt, int splits, float4* __restrict__ part,
+         int* status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -301,6 +308,8 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
   const int za = bt.a_batched ? item : 0, zb = bt.b_batched ? item : 0;
   C += item * bt.stride_c;
   const int T = (K + XK - 1) / XK;
+  const int split = int(blockIdx.y);
+  const int t0 = split * T / splits, nT = (split + 1) * T / splits - t0;
 
   if (tid == 0) {
     for (int s = 0; s < XSTAGES; ++s) {
@@ -326,7 +335,7 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
   if (warp == 0) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      for (int t = 0; t < T && !*abort_flag; ++t) {
+      for (int t = 0; t < nT && !*abort_flag; ++t) {
         const int s = t % XSTAGES;
         if (t >= XSTAGES &&
             !mbar_wait_bounded(empty0 + 8 * s, ((t / XSTAGES) - 1) & 1, status,
@@ -336,15 +345,15 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
         }
         const uint32_t bar = full0 + 8 * s;
         mbar_arrive_expect_tx(bar, X_A_BYTES + X_B_BYTES);
-        load_stage<OA, OB>(A_of(s), B_of(s), &tmA, &tmB, t, m0, n0, za, zb,
-                           bar);
+        load_stage<OA, OB>(A_of(s), B_of(s), &tmA, &tmB, t0 + t, m0, n0, za,
+                           zb, bar);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_tf32(XM, XN, false, false);
-      for (int t = 0; t < T; ++t) {
+      for (int t = 0; t < nT; ++t) {
         const int s = t % XSTAGES;
         if (*abort_flag ||
             !mbar_wait_bounded(conv0 + 8 * s, (t / XSTAGES) & 1, status,
@@ -378,7 +387,7 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ---------------------------------------------------------- split
     const int ct = tid - 64;  // 0..127
-    for (int t = 0; t < T; ++t) {
+    for (int t = 0; t < nT; ++t) {
       const int s = t % XSTAGES;
       if (*abort_flag ||
           !mbar_wait_bounded(full0 + 8 * s, (t / XSTAGES) & 1, status,
@@ -400,13 +409,28 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
     const int quarter = warp & 3;  // this warp's tensor-memory lanes
     const int r = m0 + 32 * quarter + lane;
     float* crow = C + (long long)r * ldc;
+    float4* piece = part + ((long long)blockIdx.x * splits + split) *
+                               (XM * XN / 4) +
+                    quarter * 4 * 8 * 32 + lane;
 #pragma unroll 1
     for (int cb = 0; cb < XN / 32; ++cb) {
       uint32_t v[32];
       tc::tmem_ld_32x32b_x32(tmem + (uint32_t(32 * quarter) << 16) + 32 * cb,
                              v);
       tc::tmem_ld_wait();
-      if (!ok || *abort_flag || r >= M) continue;
+      if (!ok || *abort_flag) continue;
+      if (splits > 1) {  // (an empty k range contributes zeros)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          __stcg(piece + (cb * 8 + e) * 32,
+                 nT == 0 ? make_float4(0.f, 0.f, 0.f, 0.f)
+                         : make_float4(__uint_as_float(v[4 * e]),
+                                       __uint_as_float(v[4 * e + 1]),
+                                       __uint_as_float(v[4 * e + 2]),
+                                       __uint_as_float(v[4 * e + 3])));
+        continue;
+      }
+      if (r >= M) continue;
       const int c0 = n0 + 32 * cb;
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
@@ -430,6 +454,44 @@ k_tf32x3(const __grid_constant__ CUtensorMap tmA,
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, X_TMEM_COLS);
+  }
+}
+
+// Adds the split-k pieces of k_tf32x3 in split order and stores C: one
+// thread per float4 of a tile (grid: tiles x 16 blocks of 256), loads
+// coalesced over the warp-major pieces.
+__global__ void __launch_bounds__(256)
+k_splitk_reduce(const float4* __restrict__ part, int splits,
+                float* __restrict__ C, int M, int N, long long ldc,
+                int tiles_m, int tiles_n, int vec_store, Scale sc,
+                long long stride_c) {
+  const int idx = int(blockIdx.y) * 256 + int(threadIdx.x);  // 0..4095
+  const int lane = idx & 31, e = (idx >> 5) & 7, cb = (idx >> 8) & 3,
+            q = idx >> 10;
+  const int tpb = tiles_m * tiles_n;
+  const int item = int(blockIdx.x) / tpb;
+  int pm, pn;
+  tile_of(int(blockIdx.x) - item * tpb, tiles_m, tiles_n, pm, pn);
+  const int r = pm * XM + 32 * q + lane;
+  const int c = pn * XN + 32 * cb + 4 * e;
+  if (r >= M || c >= N) return;
+  const float4* src = part + (long long)blockIdx.x * splits * (XM * XN / 4) + idx;
+  float4 acc = __ldcg(src);
+  for (int sp = 1; sp < splits; ++sp) {
+    const float4 x = __ldcg(src + (long long)sp * (XM * XN / 4));
+    acc.x += x.x;
+    acc.y += x.y;
+    acc.z += x.z;
+    acc.w += x.w;
+  }
+  float* crow = C + item * stride_c + (long long)r * ldc;
+  if (vec_store && c + 3 < N) {
+    *reinterpret_cast<float4*>(crow + c) = epi4(acc, crow + c, sc);
+  } else {
+    const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (c + u < N) crow[c + u] = epi1(v[u], crow + c + u, sc);
   }
 }
 
@@ -1475,9 +1537,28 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   }
 }
 
+int plan_tf32x3_splits(int64_t M, int64_t N, int64_t K, int64_t batch,
+                       int sms) {
+  // Split k when the tiles fill under half of the SMs: up to the SMs the
+  // tiles leave idle, at least 2 k-slices a split, at most 16 splits.
+  const int64_t tiles = batch * ((M + XM - 1) / XM) * ((N + XN - 1) / XN);
+  const int64_t T = (K + XK - 1) / XK;
+  if (tiles <= 0 || 2 * tiles > sms) return 1;
+  int64_t sp = sms / tiles;
+  if (sp > T / 2) sp = T / 2;
+  if (sp > 16) sp = 16;
+  return sp < 2 ? 1 : int(sp);
+}
+
+size_t tf32x3_split_floats(int64_t M, int64_t N, int64_t batch, int splits) {
+  if (splits <= 1) return 0;
+  return size_t(batch) * size_t((M + XM - 1) / XM) * size_t((N + XN - 1) / XN) *
+         size_t(splits) * XM * XN;
+}
+
 cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
-                          const CUtensorMap& tmB, int* status,
-                          cudaStream_t s) {
+                          const CUtensorMap& tmB, int* status, cudaStream_t s,
+                          int splits, float* part) {
   const int tiles_m = int((g.M + XM - 1) / XM);
   const int tiles_n = int((g.N + XN - 1) / XN);
   const bool vec = (g.ldc % 4 == 0) &&
@@ -1489,10 +1570,12 @@ cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
   bt.a_batched = g.batch > 1 && g.stride_a != 0;
   bt.b_batched = g.batch > 1 && g.stride_b != 0;
   bt.stride_c = (long long)g.stride_c;
+  if (splits < 1 || part == nullptr) splits = 1;
+  float4* part4 = reinterpret_cast<float4*>(part);
   auto go = [&](auto kernel) {
-    kernel<<<grid, X_THREADS, X_SMEM, s>>>(
+    kernel<<<dim3(grid, unsigned(splits)), X_THREADS, X_SMEM, s>>>(
         tmA, tmB, g.C, int(g.M), int(g.N), int(g.K), (long long)g.ldc,
-        tiles_m, tiles_n, vec ? 1 : 0, g.sc, bt, status);
+        tiles_m, tiles_n, vec ? 1 : 0, g.sc, bt, splits, part4, status);
   };
   switch (g.op_a * 2 + g.op_b) {
     case 0: go(k_tf32x3<0, 0>); break;
@@ -1500,6 +1583,11 @@ cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
     case 2: go(k_tf32x3<1, 0>); break;
     default: go(k_tf32x3<1, 1>); break;
   }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || splits == 1) return e;
+  k_splitk_reduce<<<dim3(grid, XM * XN / 4 / 256), 256, 0, s>>>(
+      part4, splits, g.C, int(g.M), int(g.N), (long long)g.ldc, tiles_m,
+      tiles_n, vec ? 1 : 0, g.sc, (long long)g.stride_c);
   return cudaGetLastError();
 }
 

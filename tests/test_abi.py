@@ -67,7 +67,8 @@ C16 = 0x7f0020000000
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc,a,b,expect", [
     (4096, 4096, 4096, 4096, 4096, 4096, A16, B16, "tf32x3_pair"),
     (256, 256, 256, 256, 256, 256, A16, B16, "tf32x3"),
-    (1024, 1024, 1024, 1024, 1024, 1024, A16, B16, "tf32x3_pair"),
+    (1024, 1024, 1024, 1024, 1024, 1024, A16, B16, "tf32x3"),  # split k
+    (1024, 1024, 4096, 4096, 1024, 1024, A16, B16, "tf32x3_pair"),
     (512, 512, 512, 512, 512, 512, A16, B16, "tf32x3"),
     (2048, 2048, 2048, 2048, 2048, 2048, A16, B16, "tf32x3_pair"),
     (512, 512, 4096, 4096, 512, 512, A16, B16, "tf32x3_pair"),  # long K: split
