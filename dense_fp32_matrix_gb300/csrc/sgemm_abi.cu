@@ -462,15 +462,24 @@ bool call_overlaps(const Call& c) {
                   c.N, c.ldc);
 }
 
+// N == 1 with A stored transposed (K x M): c^T = b^T A_stored is a row
+// vector times a row-major matrix, streamed by the M == 1 kernel without a
+// transposed copy of A, when c and b are contiguous.
+bool gemv_col_as_row(const Call& c) {
+  return c.N == 1 && c.op_a && c.ldc == 1 && (c.op_b || c.ldb == 1);
+}
+
 // Host-only path choice (no device access): the kernel that computes the
 // products. AUTO when no kernel runs (empty C, or nothing to multiply).
 int plan_call(const Call& c) {
   if (c.M == 0 || c.N == 0 || !reads_ab(c)) return SGEMM_PATH_AUTO;
   const uint64_t a = reinterpret_cast<uint64_t>(c.A);
   const uint64_t b = reinterpret_cast<uint64_t>(c.B);
-  // c = a * B^T is a product of B's rows with a: the N == 1 kernel.
+  // c = a * B^T is a product of B's rows with a: the N == 1 kernel; and
+  // c = A^T b (A stored K x M) is the row b^T A: the M == 1 kernel.
   if (c.M == 1) return c.op_b ? SGEMM_PATH_GEMV_COL : SGEMM_PATH_GEMV_ROW;
-  if (c.N == 1) return SGEMM_PATH_GEMV_COL;
+  if (c.N == 1)
+    return gemv_col_as_row(c) ? SGEMM_PATH_GEMV_ROW : SGEMM_PATH_GEMV_COL;
   const int64_t tiles = ((c.M + kTileM - 1) / kTileM) *
                         ((c.N + kTileN - 1) / kTileN);
   // Operands the tensor maps cannot take (row stride or base not 16-byte
@@ -623,6 +632,14 @@ int run_call(const Call& call, void* stream, int path) {
       return rc != SGEMM_OK ? rc : to_status(e);
     }
     case SGEMM_PATH_GEMV_ROW: {
+      if (call.M != 1 && gemv_col_as_row(call)) {
+        // c^T (1 x M) = b^T (1 x K) * A_stored (K x M, row pitch lda)
+        GemmArgs h{1, call.M, call.K, call.B, std::max<int64_t>(call.K, 1),
+                   call.A, call.lda, call.C, std::max<int64_t>(call.M, 1)};
+        h.sc = g.sc;
+        const cudaError_t e = run_gemv_row(h, *st, s, &rc);
+        return rc != SGEMM_OK ? rc : to_status(e);
+      }
       if (call.M != 1) return SGEMM_ERR_PATH;
       rc = make_row_major(g, *st, s);
       if (rc != SGEMM_OK) return rc;

@@ -148,7 +148,10 @@ def test_sgemm_rejects_bad_arguments_before_touching_a_device(lib):
     ("N", "T", 100, 20, 64, 64, 64, A16 + 4, B16, "tiled_ldg"),
     ("N", "T", 1, 4096, 4096, 4096, 4096, A16, B16, "gemv_col"),  # a * B^T
     ("T", "N", 1, 4096, 4096, 1, 4096, A16, B16, "gemv_row"),
-    ("T", "N", 4096, 1, 4096, 4096, 1, A16, B16, "gemv_col"),
+    # c = A^T b with dense c and b: the row kernel on A as stored
+    ("T", "N", 4096, 1, 4096, 4096, 1, A16, B16, "gemv_row"),
+    ("T", "T", 4096, 1, 4096, 4096, 4096, A16, B16, "gemv_row"),
+    ("N", "N", 4096, 1, 4096, 4096, 1, A16, B16, "gemv_col"),
     ("N", "N", 5, 5, 0, 1, 5, 0, 0, "auto"),            # K = 0: scale only
 ])
 def test_plan_ex(lib, op_a, op_b, M, N, K, lda, ldb, a, b, expect):

@@ -170,3 +170,40 @@ def test_pair_matches_one_sm_kernel_bitwise(ops):
         outs.append(C)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1])
+
+
+# c = A^T b with A stored K x M and dense c, b: the M == 1 kernel streams A
+# as stored (c^T = b^T A), no transposed copy. Both forms of b, alpha/beta,
+# ragged sizes, a row pitch with padding (lda > M), and an unaligned pitch
+# (the plain-load row kernel).
+@pytest.mark.parametrize("op_b", ["N", "T"])
+@pytest.mark.parametrize("M,K,lda_pad", [(4096, 4096, 0), (1000, 3000, 4),
+                                         (37, 5000, 3), (3001, 17, 0)],
+                         ids=str)
+@pytest.mark.parametrize("kind,alpha,beta", [("integers", 0.5, 2.0),
+                                             ("uniform", 1.0, 0.0)])
+def test_transposed_a_times_vector(op_b, M, K, lda_pad, kind, alpha, beta):
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    gen = matgen.KINDS[kind]
+    A = gen(5, matgen.MATRIX_A, M, K)
+    b = gen(5, matgen.MATRIX_B, K, 1)
+    C0 = gen(5, 2, M, 1)
+    A_st = np.ascontiguousarray(A.T)                    # K x M
+    lda = M + lda_pad
+    assert dfm.sgemm_plan_ex("T", op_b, M, 1, K, lda, K if op_b == "T" else 1,
+                             1, 0x7f0000000000, 0x7f0010000000,
+                             0x7f0020000000) == "gemv_row"
+    dA = torch.full((K, lda), float("nan"), device="cuda")
+    dA[:, :M] = torch.from_numpy(A_st)
+    db = torch.from_numpy(np.ascontiguousarray(b.ravel())).cuda()
+    dC = torch.from_numpy(np.ascontiguousarray(C0.ravel())).cuda()
+    dfm.sgemm_ex("T", op_b, M, 1, K, alpha, dA, lda, db,
+                 K if op_b == "T" else 1, beta, dC, 1)
+    torch.cuda.synchronize()
+    assert dfm.sgemm_watchdog_status() == (0, 0)
+    ref, S = oracle.gemm_ex("T", op_b, alpha, A_st,
+                            b.reshape(1, K) if op_b == "T" else b, beta, C0,
+                            M, 1, K)
+    compare(kind, dC.cpu().numpy().reshape(M, 1), ref, S,
+            "A^T b %dx%d %s" % (M, K, op_b))
