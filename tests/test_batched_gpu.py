@@ -116,3 +116,16 @@ def test_batch_of_one_matches_sgemm_ex_bitwise():
                               C2, N, M * N, 1)
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
+
+
+# A batch whose pair schedule has whole tiles and a stream-K tail (8 items
+# of 4 x 4 tiles = 128 tiles on 76 clusters): the split tiles' pieces are
+# summed under the whole tiles' MMAs and written straight to C, the whole
+# tiles' accumulators are parked half in tensor memory; items of C stacked
+# or side by side, with and without beta.
+@pytest.mark.parametrize("side", [False, True])
+@pytest.mark.parametrize("kind,alpha,beta", [("integers", 0.5, 2.0),
+                                             ("uniform", 1.0, 0.0)])
+def test_pair_batch_with_split_tail(side, kind, alpha, beta):
+    run_batch(("N", "N"), 1024, 1024, 640, 8, alpha=alpha, beta=beta,
+              kind=kind, seed=21, path="tf32x3_pair", side_by_side=side)
