@@ -27,8 +27,9 @@ std::atomic<int> g_math_mode{SGEMM_MATH_AUTO};
 constexpr int64_t kTf32RepackMinMacs = int64_t(1) << 24;
 // From this much work on (256 x 256 tiles x k-slices of 32) the 2-SM pair
 // kernel, which splits k-slices over all clusters when tiles are few, beats
-// one 1-SM block per 128 x 128 tile (measured: 1024^3 and every long-K
-// shape of few tiles go to pairs, 512^3 stays on single blocks).
+// one 1-SM block per 128 x 128 tile (measured: every long-K shape of few
+// tiles goes to pairs, 512^3 stays on single blocks), except for the short-k
+// few-tile products below.
 constexpr int64_t kTf32PairMinWork = 256;
 // Below this many 128 x 128 tiles (half of GB300's 152 SMs) single blocks
 // split k over the idle SMs; with short k (up to this many k-slices) that

@@ -20,7 +20,7 @@
 //   warps 2..5  split each landed stage: A elementwise in place (hi) and
 //               into the A_lo buffer; B transposed as well (below); then
 //               after the last stage read the accumulator from tensor
-//               memory and store C;
+//               memory and store C (or, with split k, the block's piece);
 //   warp 1      allocates 128 tensor-memory columns and issues the MMAs
 //               (M = 128, N = 128, K = 8 per instruction) from one thread,
 //               releasing each stage with tcgen05.commit.
@@ -31,6 +31,8 @@
 // warp owns one 32 x 32 box: every lane gathers one column n across the 32 k
 // rows, then the warp writes the box back in place as 32 K-major rows (hi)
 // and the matching rows of B_lo. Same 4 KiB footprint, no extra buffer.
+// Products with few tiles split k over the idle SMs (k_splitk_reduce adds
+// the pieces in order).
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -509,15 +511,18 @@ k_splitk_reduce(const float4* __restrict__ part, int splits,
 // c + i G to cluster c); the k-slices of the remaining tiles (fewer than one
 // wave, or one wave more when that share would be short) are split evenly
 // over all G clusters, so no partly filled last wave is left. A cluster's
-// share is a run of k-ranges ("units"); a unit that covers its whole tile
-// stores C directly, a partial one writes its fp32 piece to the workspace
-// and the last of the tile's pieces to arrive adds them all in k order and
-// stores C (no cluster waits on another; the sum order is fixed).
+// share is a run of k-ranges ("units"), taken before its whole tiles; a unit
+// that covers its whole tile stores C directly, a partial one writes its
+// fp32 piece to the workspace and the last of the tile's pieces to arrive
+// adds them all in k order and stores C (no cluster waits on another; the
+// sum order is fixed).
 //
 // Roles in each block (448 threads):
 //   warp 0      TMA producer over the cluster's units, one ring of stages;
-//   warp 1      even block: allocates 512 tensor-memory columns (two
-//               256-column accumulators) for both blocks and issues the
+//   warp 1      even block: allocates 512 tensor-memory columns for both
+//               blocks (row-major A: one 256-column accumulator, four
+//               32-column A_lo stages and 128 columns for a parked half
+//               accumulator; transposed A: two accumulators) and issues the
 //               MMAs; odd block: forwards each completed split to the even
 //               block with one arrival per stage;
 //   warps 2..9  split and transpose each landed stage and arrive on their
@@ -527,7 +532,10 @@ k_splitk_reduce(const float4* __restrict__ part, int splits,
 //   warps 10..13 epilogue, one tensor-memory lane quarter each: read a
 //               finished accumulator, store C or the piece, hand the
 //               accumulator back. With two accumulators the MMAs of the
-//               next unit run while the previous one is stored.
+//               next unit run while the previous one is stored; with one,
+//               its upper half is parked in tensor memory first and stored
+//               after the hand-back. They also sum the split tiles' pieces
+//               (under the next whole tile's MMAs when one follows).
 constexpr int PM = 256, PN = 256;
 constexpr int P_THREADS = 448;
 constexpr int P_PREFETCH = 3;                        // k-slices ahead into L2
