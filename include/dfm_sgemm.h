@@ -90,7 +90,8 @@ extern "C" {
 #define SGEMM_PATH_AUTO 0
 #define SGEMM_PATH_TILED_TMA 1  /* TMA-fed multistage tile kernel (aligned) */
 #define SGEMM_PATH_TILED_LDG 2  /* same tile core, 4-byte async loads     */
-#define SGEMM_PATH_GEMV_ROW 3   /* M == 1: c = a * B, column blocks       */
+#define SGEMM_PATH_GEMV_ROW 3   /* M == 1: c = a * B, column blocks (also
+                                   c = A^T b as c^T = b^T A, sgemm_ex)     */
 #define SGEMM_PATH_GEMV_COL 4   /* N == 1: c = A * b, one warp per row     */
 #define SGEMM_PATH_NAIVE 5      /* one thread per output (debug baseline)  */
 #define SGEMM_PATH_TF32X3 6     /* tensor cores, 3 TF32 products (aligned)  */
@@ -139,7 +140,11 @@ int sgemm_path(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
  *                            + |beta * C_old|) + 1e-6.
  * The tensor-core kernels read transposed operands in place; the CUDA-core
  * kernels get row-major copies made in the stream's workspace (a
- * bandwidth-bound transpose, grown like the stream-K workspace).
+ * bandwidth-bound transpose, grown like the stream-K workspace). The
+ * vector shapes need no copy: with M == 1, c = a * op(B) streams B as
+ * stored; with N == 1, op_a == SGEMM_OP_T and contiguous c and b (ldc == 1,
+ * b a row or a column with ldb == 1), c = A^T b streams A as stored as the
+ * row product c^T = b^T A.
  * Errors: as sgemm, plus SGEMM_ERR_INVALID_VALUE for an unknown op.
  */
 int sgemm_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K,
