@@ -230,3 +230,39 @@ def test_pair_early_fixup_epilogue(pad, ops, kind, alpha, beta):
                                      ((300, 203, 64), 208)], ids=str)
 def test_pair_never_writes_past_row_end(mnk, ldc):
     run_case(*mnk, kind="integers", seed=5, ldc=ldc, path=PAIR)
+
+
+# Few tiles: the single-block kernel splits k over the idle SMs and a
+# second kernel adds the pieces in order (alpha, beta, ragged edges,
+# transposed forms and batches all go through the reduce kernel).
+@pytest.mark.parametrize("ops", [("N", "N"), ("N", "T"), ("T", "N"), ("T", "T")],
+                         ids="".join)
+@pytest.mark.parametrize("kind,alpha,beta", [("integers", 0.5, 2.0),
+                                             ("uniform", -1.25, 0.5),
+                                             ("uniform", 1.0, 0.0)])
+def test_split_k_single_blocks(ops, kind, alpha, beta):
+    from test_ex_gpu import run_ex
+    run_ex(*ops, 700, 300, 900, alpha, beta, kind=kind, seed=3, path=PATH)
+    run_ex(*ops, 129, 1000, 4000, alpha, beta, kind=kind, seed=4, path=PATH,
+           pad=1)
+
+
+@pytest.mark.parametrize("side", [False, True])
+def test_split_k_batches(side):
+    from test_batched_gpu import run_batch
+    run_batch(("N", "N"), 200, 300, 640, 3, alpha=0.5, beta=2.0,
+              kind="integers", seed=8, path=PATH, side_by_side=side)
+    run_batch(("T", "N"), 257, 129, 1000, 2, kind="uniform", seed=9,
+              path=PATH, shared_b=True, side_by_side=side)
+
+
+def test_split_k_matches_unsplit_bitwise_on_integers():
+    # integer data: every split and the single pass are exact, so equal
+    import torch
+    import dense_fp32_matrix_gb300 as dfm
+    A = torch.from_numpy(matgen.integers(12, 0, 512, 2048)).cuda()
+    B = torch.from_numpy(matgen.integers(12, 1, 2048, 384)).cuda()
+    C = dfm.matmul(A, B, path=PATH)       # 12 tiles: split k
+    ref = (A.double() @ B.double()).float()
+    torch.cuda.synchronize()
+    assert torch.equal(C, ref)
