@@ -175,17 +175,6 @@ __device__ __forceinline__ void bulk_wait_group_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Prefetch the 2-D box at {x, y} of the tensor map into L2 (no shared
-// memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map,
-                                                   int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(x), "r"(y)
-      : "memory");
-}
-
 // 2-D tiled bulk tensor load global -> shared, completion signalled on the
 // mbarrier as transaction bytes. x is the innermost coordinate (elements),
 // y the outer one. Out-of-bounds box elements are filled with zero.
@@ -267,13 +256,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
 
 __device__ __forceinline__ void mbar_inval(uint32_t bar) {
   asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// 16-byte asynchronous copy global -> shared, cached in L2 only.
-__device__ __forceinline__ void cp_async_16_cg(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
-               "l"(src)
-               : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() {

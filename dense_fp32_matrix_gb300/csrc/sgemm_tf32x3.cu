@@ -175,8 +175,9 @@ __device__ __forceinline__ void split_transpose_half(uint8_t* box,
 
 // ------------------------------------------------- operand layouts (op)
 //
-// Both MMA operands must be K-major (reading 14 of the design notes). Per
-// operand the stored layout decides the work:
+// Both MMA operands are presented K-major: on this part a kind::tf32 MMA
+// with either MN-major descriptor bit set returned zeros. Per operand the
+// stored layout decides the work:
 //   A, op_a == 0 (stored M x K) and B, op_b == 1 (stored N x K): K-major
 //     already; one TMA box {32 k, 128 rows} lands in the canonical
 //     128-byte-swizzled layout and only the low part is split off.
@@ -1502,8 +1503,11 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   p.sk_iters = (long long)pl.sk_iters;
   p.ws = ws;
   p.counters = counters;
+  // 16-byte stores need every item's rows on 16 bytes: the base, the row
+  // pitch and, for a batch, the item stride.
   p.vec_store = (g.ldc % 4 == 0) &&
-                (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
+                (reinterpret_cast<uintptr_t>(g.C) % 16 == 0) &&
+                (g.batch <= 1 || g.stride_c % 4 == 0);
   p.sc = g.sc;
   p.tma_c = tmC != nullptr && g.sc.beta == 0.f;
   const CUtensorMap& mapC = p.tma_c ? *tmC : tmA;  // unused without tma_c
@@ -1570,7 +1574,8 @@ cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
   const int tiles_m = int((g.M + XM - 1) / XM);
   const int tiles_n = int((g.N + XN - 1) / XN);
   const bool vec = (g.ldc % 4 == 0) &&
-                   (reinterpret_cast<uintptr_t>(g.C) % 16 == 0);
+                   (reinterpret_cast<uintptr_t>(g.C) % 16 == 0) &&
+                   (g.batch <= 1 || g.stride_c % 4 == 0);
   const unsigned grid = unsigned(g.batch) * unsigned(tiles_m) *
                         unsigned(tiles_n);  // < 2^31, checked by the host
   Batch bt;

@@ -129,3 +129,15 @@ def test_batch_of_one_matches_sgemm_ex_bitwise():
 def test_pair_batch_with_split_tail(side, kind, alpha, beta):
     run_batch(("N", "N"), 1024, 1024, 640, 8, alpha=alpha, beta=beta,
               kind=kind, seed=21, path="tf32x3_pair", side_by_side=side)
+
+
+# Items side by side whose column offset (the item stride) is not a multiple
+# of 4 floats while the row pitch is: item 1 starts 24 or 40 bytes into the
+# row, so the kernels must fall back from 16-byte stores of C for every item.
+@pytest.mark.parametrize("path", ["auto", "tf32x3", "tf32x3_pair"])
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_side_by_side_item_stride_off_16_bytes(path, beta):
+    run_batch(("N", "T"), 300, 6, 64, 2, beta=beta, kind="integers", seed=22,
+              path=path, side_by_side=True)
+    run_batch(("T", "T"), 132, 10, 36, 2, beta=beta, kind="uniform", seed=23,
+              path=path, side_by_side=True)

@@ -150,3 +150,29 @@ def test_integer_inputs_fp32_rounding_is_exact():
 
 def test_threads_reported():
     assert oracle.num_threads() >= 1
+
+
+# -- the inner-product and outer-product formulations agree ------------------
+# hotelren.com, section 1.3: reordering the loops into rank-1 updates does
+# not change the mathematical result. Both orders form each exact fp64
+# product and add them per output in ascending k, so on float data (not just
+# integers) the two results and the two absolute sums agree bit for bit.
+
+@pytest.mark.parametrize("kind", ["uniform", "normal"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (7, 5, 3), (33, 17, 65),
+                                   (64, 96, 300), (129, 31, 1023)])
+def test_inner_equals_outer_bitwise_on_floats(kind, M, N, K):
+    A = matgen.KINDS[kind](70 + K, matgen.MATRIX_A, M, K)
+    B = matgen.KINDS[kind](70 + K, matgen.MATRIX_B, K, N)
+    ci, si = oracle.gemm(A, B, order="inner")
+    co, so = oracle.gemm(A, B, order="outer")
+    assert np.array_equal(ci.view(np.uint64), co.view(np.uint64))
+    assert np.array_equal(si.view(np.uint64), so.view(np.uint64))
+    # and the row / entry subsets used for large shapes are the same sums
+    rows = np.array([0, M - 1], dtype=np.int64)
+    cr, sr = oracle.gemm_rows(A, B, rows)
+    assert np.array_equal(cr, co[rows]) and np.array_equal(sr, so[rows])
+    ii = np.array([0, M - 1, M // 2], dtype=np.int64)
+    jj = np.array([N - 1, 0, N // 2], dtype=np.int64)
+    ce, se = oracle.gemm_entries(A, B, ii, jj)
+    assert np.array_equal(ce, co[ii, jj]) and np.array_equal(se, so[ii, jj])
