@@ -10,11 +10,16 @@ every step, outside the timed events. Reported:
   value      TFLOP/s = 2 M N K / mean device time of a step (CUDA events on
              the launching stream), summed over ranks (replicas);
   roofline   the bound of the kernel the step runs: "tensor" for the 3xTF32
-             kernels (the measured bf16 GEMM peak scaled to TF32 and divided
-             by the 3 products per fp32 product), "hbm" for the vector shapes
+             kernels (the dense TF32 tensor rate, SMs x 4096 ops/clk x the
+             median SM clock sampled inside the timed region, divided by the
+             3 products per fp32 product; the measured bf16 burst scaled to
+             TF32 is given beside it as context), "hbm" for the vector shapes
              (algorithmic bytes against the measured copy bandwidth), "alu"
              for the FFMA kernels (SMs x 128 FMA/clk x 2 flop x the median SM
-             clock sampled during the timed region);
+             clock sampled inside the timed region);
+  ffma_kernel  the CUDA-core FFMA kernel on the same inputs, timed the same
+             way with its own clock record, as a fraction of the FP32 FMA
+             peak at that clock;
   e2e        the same metric through sgemm_host(): pinned host A, B in,
              host C out, copies inside the timed region;
   cpu_baseline  the CPU oracle timed on this host's cores on a bounded row
@@ -47,8 +52,7 @@ BF16_FALLBACK_TFLOPS = 1900.0   # used only when no measured peak is present
 HBM_FALLBACK_GBS = 6800.0
 TF32X3_PRODUCTS = 3             # TF32 tensor products per fp32 product
 # Dense TF32 tensor-core rate of one SM, ops per clock, as ncu reports it
-# for this part (the peak_sustained of the TF32 tensor-op counter; see
-# profiles/k_tf32x3_pair_square_4096.md).
+# for this part (the peak_sustained of its TF32 tensor-op counter).
 TF32_OPS_PER_CLK_PER_SM = 4096
 
 
@@ -101,34 +105,50 @@ def recorded_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock and throttle reasons while running.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Samples every 25 ms with nvidia-smi's own timestamps; ``window()`` marks
+    the host-side start and end of the timed region (the end taken after
+    the device synchronised), and the summary keeps the samples inside it,
+    so the median is the clock under load, not the idle clock around it.
+    """
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 25
 
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
         self.lines = []
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev),
                  "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms",
+                 str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         time.sleep(0.3)
         return self
 
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.15)
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -138,31 +158,46 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
         return False
 
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        try:
+            return datetime.datetime.strptime(
+                text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
         if not self.lines:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
                     "samples": 0, "note": "nvidia-smi unavailable"}
-        sm, smax, power, reasons = [], [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
         for line in self.lines:
             p = [x.strip() for x in line.split(",")]
             try:
-                sm.append(float(p[0]))
-                smax.append(float(p[1]))
-                power.append(float(p[2]))
+                rows.append((self._stamp(p[0]), float(p[1]), float(p[2]),
+                             float(p[3]), [n for n, v in zip(names, p[5:9])
+                                           if v.lower() == "active"]))
             except (ValueError, IndexError):
                 continue
-            for name, v in zip(names, p[4:8]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        # samples under load: the kernel keeps the SM clock up; idle samples at
-        # the edges of the window are dropped by taking the upper half.
-        loaded = sorted(sm)[len(sm) // 2:] if sm else []
-        return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+        inside = [r for r in rows if r[0] is not None and self.t0 is not None
+                  and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        basis = "samples inside the timed region"
+        if not inside:
+            # no stamp inside (a very short region): the upper half of all
+            # samples, as the kernel keeps the SM clock up while it runs
+            inside = sorted(rows, key=lambda r: r[1])[len(rows) // 2:]
+            basis = "upper half of the samples around the timed region"
+        sm = [r[1] for r in inside]
+        reasons = sorted({n for r in inside for n in r[4]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(r[2] for r in rows) if rows else None,
+                "reasons": reasons, "samples": len(rows),
+                "samples_in_region": len(sm), "basis": basis,
+                "sm_mhz_min": min(sm) if sm else None,
+                "power_w_max": max(r[3] for r in inside) if inside else None}
 
 
 def measured_bf16_tflops():
@@ -203,8 +238,9 @@ class L2Flush:
         torch.sum(self.r, dim=(0,), out=self.sink)
 
 
-def time_steps(step, flush, stream, n, warmup):
-    """Per-step device times (ms) with an L2 flush before each step."""
+def time_steps(step, flush, stream, n, warmup, sampler=None):
+    """Per-step device times (ms) with an L2 flush before each step; the
+    clock sampler (if any) is told where the timed region starts and ends."""
     import torch
     for _ in range(warmup):
         flush()
@@ -212,12 +248,16 @@ def time_steps(step, flush, stream, n, warmup):
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    if sampler is not None:
+        sampler.start()
     for i in range(n):
         flush()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.stop()
     return [a.elapsed_time(b) for a, b in ev]
 
 
@@ -378,12 +418,14 @@ def run_gpu(args, w):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev) as clocks:
+        clocks.start()
         for i in range(args.steps):
             flush()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
+        clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     st, site = dfm.sgemm_watchdog_status()
@@ -431,41 +473,52 @@ def run_gpu(args, w):
     if not bool(((hC - C.cpu()).abs() <= 2e-4 * s_bound + 2e-6).all()):
         raise RuntimeError("e2e result differs from the device-path result")
 
-    # The FP32 FMA roofline of this GPU at the clock seen while timing.
-    peak_clock_mhz = clk["sm_mhz"] or (clk["sm_max_mhz"] or 2070.0)
-    ffma_peak = sms * FMA_PER_CLK_PER_SM * 2 * peak_clock_mhz * 1e6 / 1e12
-    ffma_basis = ("%d SMs x %d FP32 FMA/clk x 2 flop x %.0f MHz (median SM "
-                  "clock sampled during the timed region)"
-                  % (sms, FMA_PER_CLK_PER_SM, peak_clock_mhz))
+    def ffma_peak_at(mhz):
+        return sms * FMA_PER_CLK_PER_SM * 2 * mhz * 1e6 / 1e12
+
+    def ffma_basis(mhz, where):
+        return ("%d SMs x %d FP32 FMA/clk x 2 flop x %.0f MHz (median SM "
+                "clock of the samples inside %s)"
+                % (sms, FMA_PER_CLK_PER_SM, mhz, where))
+
+    # The clock of the timed region (its median under load).
+    clock_mhz = clk["sm_mhz"] or (clk["sm_max_mhz"] or 2070.0)
     kernel = {"tiled_tma": "k_tiled_tma", "tiled_ldg": "k_tiled_ldg",
               "tf32x3": "k_tf32x3", "tf32x3_pair": "k_tf32x3_pair",
               "gemv_row": "k_gemv_row_tma", "gemv_col": "k_gemv_col_tma"}.get(
                   plan, plan)
     if plan.startswith("tf32x3"):
+        # Roofline of the tensor kernels: the dense TF32 rate of the tensor
+        # cores at the SM clock of the timed region (ncu's per-clock rate of
+        # the TF32 tensor-op counter), in fp32 work: each fp32 product is
+        # 3 TF32 products. The measured bf16 burst scaled by the nominal
+        # TF32/BF16 ratio is given beside it as context only: that burst
+        # ran under the power cap at a much lower clock than these kernels
+        # do, so it is not a ceiling for them.
+        hw_peak = sms * TF32_OPS_PER_CLK_PER_SM * clock_mhz * 1e6 / 1e12
+        eff_peak = hw_peak / TF32X3_PRODUCTS
         bf16, src = measured_bf16_tflops()
-        tf32_peak = bf16 * TF32_PER_BF16
-        eff_peak = tf32_peak / TF32X3_PRODUCTS
+        tf32_from_bf16 = bf16 * TF32_PER_BF16
         roof = {"bound": "tensor", "achieved": tflops, "peak": eff_peak,
                 "unit": "TFLOP/s", "frac": tflops / eff_peak,
                 "traffic": recorded_traffic(kernel, w["name"]),
                 "kernel": kernel,
-                "peak_basis": ("TF32 dense tensor peak = bf16 burst %.1f "
-                               "TFLOP/s (%s, MEASURED_PEAKS.json) x nominal "
-                               "TF32/BF16 ratio 1.1/2.25 = %.1f TFLOP/s; "
-                               "3 TF32 products per fp32 product -> %.1f "
-                               "TFLOP/s of fp32 work" % (bf16, src, tf32_peak,
-                                                         eff_peak)),
+                "peak_basis": ("dense TF32 tensor rate %d SMs x %d ops/clk "
+                               "(ncu) x %.0f MHz (median SM clock inside the "
+                               "timed region) = %.1f TFLOP/s of TF32; 3 TF32 "
+                               "products per fp32 product -> %.1f TFLOP/s of "
+                               "fp32 work" % (sms, TF32_OPS_PER_CLK_PER_SM,
+                                              clock_mhz, hw_peak, eff_peak)),
                 "tensor_tflops": TF32X3_PRODUCTS * tflops,
-                "tensor_peak": tf32_peak}
-        # The same work against the hardware's dense TF32 rate at the SM
-        # clock seen while timing (what ncu's tensor-pipe counter measures):
-        # a fraction that cannot exceed 1.
-        hw_peak = sms * TF32_OPS_PER_CLK_PER_SM * peak_clock_mhz * 1e6 / 1e12
-        roof["tensor_pipe"] = {
-            "peak_tflops": hw_peak,
-            "frac": TF32X3_PRODUCTS * tflops / hw_peak,
-            "basis": ("%d SMs x %d dense TF32 ops/clk (ncu) x %.0f MHz"
-                      % (sms, TF32_OPS_PER_CLK_PER_SM, peak_clock_mhz))}
+                "tensor_peak": hw_peak,
+                "context_bf16_derived": {
+                    "peak": tf32_from_bf16 / TF32X3_PRODUCTS,
+                    "frac": tflops / (tf32_from_bf16 / TF32X3_PRODUCTS),
+                    "basis": ("bf16 burst %.1f TFLOP/s (%s, "
+                              "MEASURED_PEAKS.json, taken under the power "
+                              "cap) x nominal TF32/BF16 ratio 1.1/2.25 / 3 "
+                              "products; context, not a ceiling"
+                              % (bf16, src))}}
     elif plan in ("gemv_row", "gemv_col"):
         # a stream over the matrix: bound by HBM bandwidth
         hbm, src = measured_hbm_gbs()
@@ -478,27 +531,52 @@ def run_gpu(args, w):
                               "MEASURED_PEAKS.json); algorithmic bytes "
                               "4(MK + KN + MN)" % (hbm, src)}
     else:
-        roof = {"bound": "alu", "achieved": tflops, "peak": ffma_peak,
-                "unit": "TFLOP/s", "frac": tflops / ffma_peak,
+        roof = {"bound": "alu", "achieved": tflops,
+                "peak": ffma_peak_at(clock_mhz), "unit": "TFLOP/s",
+                "frac": tflops / ffma_peak_at(clock_mhz),
                 "traffic": recorded_traffic(kernel, w["name"]),
-                "kernel": kernel, "peak_basis": ffma_basis}
+                "kernel": kernel,
+                "peak_basis": ffma_basis(clock_mhz, "the timed region")}
 
-    # The CUDA-core FFMA kernel on the same inputs, timed the same way.
+    # The CUDA-core FFMA kernel on the same inputs, timed the same way, with
+    # its own clock record: its roofline is the FP32 FMA peak at the clock
+    # seen while it ran.
     ffma = None
     if plan.startswith("tf32x3") and not args.no_ffma:
         prev = dfm.sgemm_set_math_mode("ffma")
         try:
             ffma_path = dfm.sgemm_plan(M, N, K, K, N, N, A.data_ptr(),
                                        B.data_ptr(), C.data_ptr())
-            fms = time_steps(step, flush, stream, max(5, min(args.steps, 100)),
-                             args.warmup)
+            with ClockSampler(dev) as fclocks:
+                fms = time_steps(step, flush, stream,
+                                 max(5, min(args.steps, 100)), args.warmup,
+                                 fclocks)
         finally:
             dfm.sgemm_set_math_mode(prev)
+        st, site = dfm.sgemm_watchdog_status()
+        if st != 0:
+            raise RuntimeError("watchdog fired in the FFMA leg (site %d)"
+                               % site)
+        fclk = fclocks.summary()
+        f_mhz = fclk["sm_mhz"] or (fclk["sm_max_mhz"] or 2070.0)
         f_ms = reduce_max(sum(fms) / len(fms), world)
         f_tflops = flops(M, N, K) / (f_ms * 1e-3) / 1e12
-        ffma = {"path": ffma_path, "value": job_tflops(flops(M, N, K), f_ms,
-                                                        world),
-                "ms_per_step": f_ms, "frac_of_ffma_peak": f_tflops / ffma_peak,
+        ffma = {"path": ffma_path, "kernel": "k_tiled_tma",
+                "value": job_tflops(flops(M, N, K), f_ms, world),
+                "unit": "TFLOP/s", "ms_per_step": f_ms,
+                "ms_min": min(fms), "ms_median": statistics.median(fms),
+                "steps": len(fms),
+                "peak": ffma_peak_at(f_mhz),
+                "frac_of_ffma_peak": f_tflops / ffma_peak_at(f_mhz),
+                "peak_basis": ffma_basis(f_mhz, "this leg's timed region"),
+                "cycles_per_step_M": f_ms * 1e-3 * f_mhz,
+                "clocks": {"sm_mhz": fclk["sm_mhz"],
+                           "sm_mhz_min": fclk.get("sm_mhz_min"),
+                           "sm_max_mhz": fclk["sm_max_mhz"],
+                           "reasons": fclk["reasons"],
+                           "samples": fclk["samples"],
+                           "samples_in_region": fclk.get("samples_in_region"),
+                           "power_w_max": fclk.get("power_w_max")},
                 "traffic": recorded_traffic("k_tiled_tma", w["name"])}
 
     line = {
@@ -516,13 +594,14 @@ def run_gpu(args, w):
                   "events)",
             "parallelism": "replicas" if world > 1 else "single GPU"}),
         "roofline": roof,
-        "pct_of_ffma_peak": 100.0 * tflops / ffma_peak,
-        "ffma_peak": {"value": ffma_peak, "unit": "TFLOP/s",
-                      "basis": ffma_basis},
         "ffma_kernel": ffma,
-        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_mhz_min": clk.get("sm_mhz_min"),
+                   "sm_max_mhz": clk["sm_max_mhz"],
                    "reasons": clk["reasons"], "samples": clk["samples"],
+                   "samples_in_region": clk.get("samples_in_region"),
+                   "basis": clk.get("basis"),
                    "power_w_max": clk.get("power_w_max")},
+        "cycles_per_step_M": ms_step * 1e-3 * clock_mhz,
         "e2e": {"value": job_tflops(flops(M, N, K), e2e_ms, world),
                 "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 4 * (M * K + K * N),
@@ -533,6 +612,8 @@ def run_gpu(args, w):
         "gpu_launches": args.steps,
         "ms_min": min(ms), "ms_median": statistics.median(ms),
     }
+    if plan in ("tiled_tma", "tiled_ldg"):
+        line["pct_of_ffma_peak"] = 100.0 * roof["frac"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, rows, sec, threads = cpu_oracle_rate(M, N, K, w["kind"],
                                                    w["seed"])

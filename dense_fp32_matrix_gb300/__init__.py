@@ -16,7 +16,7 @@ __all__ = [
     "sgemm_ex", "sgemm_plan_ex", "sgemm_strided_batched", "OPS",
     "sgemm_noalloc", "sgemm_set_math_mode", "MATH",
     "sgemm_watchdog_status", "sgemm_watchdog_selftest",
-    "sgemm_status_string", "sgemm_path_name", "sgemm_version", "matmul",
+    "sgemm_workspace_info", "sgemm_status_string", "sgemm_path_name", "sgemm_version", "matmul",
     "PATHS", "STATUS",
 ]
 
@@ -175,6 +175,16 @@ def sgemm_watchdog_status() -> tuple[int, int]:
 def sgemm_watchdog_selftest(stream=None, timeout_ns=50_000_000) -> int:
     return int(_native.lib().sgemm_watchdog_selftest(_stream(stream),
                                                      int(timeout_ns)))
+
+
+def sgemm_workspace_info() -> tuple[int, int]:
+    """(count, bytes) of the workspaces held on the current device."""
+    count = ctypes.c_int(0)
+    nbytes = ctypes.c_int64(0)
+    _check(_native.lib().sgemm_workspace_info(ctypes.byref(count),
+                                              ctypes.byref(nbytes)),
+           "sgemm_workspace_info")
+    return count.value, nbytes.value
 
 
 def sgemm_status_string(status: int) -> str:

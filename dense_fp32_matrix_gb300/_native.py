@@ -51,6 +51,8 @@ _SIGNATURES = {
     "sgemm_set_math_mode": ([_int], _int),
     "sgemm_watchdog_status": ([ctypes.POINTER(_int)], _int),
     "sgemm_watchdog_selftest": ([_vp, _i64], _int),
+    "sgemm_workspace_info": ([ctypes.POINTER(_int), ctypes.POINTER(_i64)],
+                             _int),
     "sgemm_status_string": ([_int], ctypes.c_char_p),
     "sgemm_path_name": ([_int], ctypes.c_char_p),
     "sgemm_version": ([], _int),

@@ -56,23 +56,19 @@ struct GemmArgs {
   int64_t stride_a = 0, stride_b = 0, stride_c = 0;
 };
 
-// Tile geometry of the main kernel (also used by the host dispatcher).
-// Block tile kTileM x kTileN, k-slices of kTileK, a kTileStages-deep ring;
-// kTileThreads threads, kTileMinBlocks resident blocks per SM; each lane
+// Tile geometry of the persistent TMA kernel (also used by the host
+// dispatcher). Block tile kTileM x kTileN, k-slices of kTileK, a
+// kTileStages-deep ring; kTileThreads threads, one block per SM; each lane
 // owns kLaneRows rows x (4 * kLaneChunks) columns of the block tile, with
 // kLanesN lanes of a warp along N.
-constexpr int kTileM = 128;
+constexpr int kTileM = 256;
 constexpr int kTileN = 128;
 constexpr int kTileK = 32;
-constexpr int kTileStages = 3;
+constexpr int kTileStages = 4;
 constexpr int kTileThreads = 256;
-constexpr int kTileMinBlocks = 2;
-constexpr int kLaneRows = 8;
+constexpr int kLaneRows = 16;
 constexpr int kLaneChunks = 2;
-constexpr int kLanesN = 4;
-
-// Dynamic shared memory of one tiled block, including alignment slack.
-size_t tiled_smem_bytes();
+constexpr int kLanesN = 8;
 
 // One-time per-device kernel attribute set-up. Returns a cudaError_t;
 // tiled_init also reports how many TMA tile blocks fit on one SM.

@@ -7,8 +7,9 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <memory>
 #include <mutex>
-#include <unordered_map>
+#include <vector>
 
 #include "dfm_sgemm.h"
 #include "kernels.h"
@@ -59,7 +60,23 @@ struct Workspace {
   size_t counters_len = 0;
   float* tr = nullptr;   // row-major copies of transposed operands
   size_t tr_floats = 0;
+  cudaStream_t stream = nullptr;  // the stream it serves now
+  cudaEvent_t done = nullptr;     // recorded after each call's launches
+  bool recorded = false;          // `done` holds a record
+  bool pinned = false;  // used inside a stream capture: a graph holds its
+                        // addresses, so it is never handed to another stream
+  uint64_t last_use = 0;
+
+  size_t bytes() const {
+    return (ws_floats + tr_floats) * sizeof(float) + counters_len * sizeof(int);
+  }
 };
+
+// Workspaces cached per device. Up to kMaxWorkspaces are kept; a call on a
+// stream that has none takes a new one while there is room, else the least
+// recently used one that no captured graph holds, after making its stream
+// wait (on the device) for that workspace's last call.
+constexpr size_t kMaxWorkspaces = 8;
 
 struct DeviceState {
   std::once_flag once;
@@ -68,11 +85,12 @@ struct DeviceState {
   int tma_blocks_per_sm = 0;
   int pair_clusters = 0;  // 2-block clusters of the pair kernel at once
   int* status = nullptr;
-  // Stream-K workspaces (partial tiles and tile counters), one per stream
-  // the library has been called on: kernels on unordered streams may run
-  // at the same time, so they must not share partial tiles or counters.
+  // Stream-K workspaces (partial tiles and tile counters) and transposed
+  // copies: kernels on unordered streams may run at the same time, so a
+  // workspace serves one stream at a time.
   std::mutex ws_mu;
-  std::unordered_map<cudaStream_t, Workspace> ws;
+  std::vector<std::unique_ptr<Workspace>> pool;
+  uint64_t tick = 0;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -142,15 +160,101 @@ int device_state(DeviceState** out) {
   return st.err;
 }
 
-// Make the workspace of stream s at least `floats` partial-tile floats and
-// `counters` tile counters; the caller holds st.ws_mu until its launch is
-// enqueued. Growing frees the old buffers (cudaFree waits for the device, so
-// kernels still using them finish first) and zeroes the new counters.
-int ensure_workspace(DeviceState& st, cudaStream_t s, size_t floats,
-                     size_t counters, Workspace** out) {
-  Workspace& w = st.ws[s];
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(s, &cs) == cudaSuccess &&
+         cs != cudaStreamCaptureStatusNone;
+}
+
+// One call's hold on the workspace of its stream: holds the device's
+// workspace lock from construction to destruction (after the call's
+// launches are enqueued) and, if the call used a workspace, records that
+// workspace's `done` event on the stream at the end.
+class Lease {
+ public:
+  Lease(DeviceState& st, cudaStream_t s) : st_(st), s_(s), lock_(st.ws_mu) {}
+  ~Lease() {
+    if (w_ == nullptr) return;
+    if (capturing(s_)) {
+      w_->pinned = true;
+    } else if (cudaEventRecord(w_->done, s_) == cudaSuccess) {
+      w_->recorded = true;
+    }
+  }
+  Lease(const Lease&) = delete;
+  Lease& operator=(const Lease&) = delete;
+
+  cudaStream_t stream() const { return s_; }
+
+  // The workspace serving this stream (taken on first use).
+  int get(Workspace** out) {
+    if (w_ == nullptr) {
+      const int rc = take();
+      if (rc != SGEMM_OK) return rc;
+    }
+    w_->last_use = ++st_.tick;
+    *out = w_;
+    return SGEMM_OK;
+  }
+
+ private:
+  int take() {
+    const bool cap = capturing(s_);
+    Workspace* w = nullptr;
+    for (auto& e : st_.pool)
+      if (e->stream == s_) w = e.get();
+    if (w == nullptr && st_.pool.size() >= kMaxWorkspaces && !cap) {
+      // hand the least recently used unpinned workspace to this stream
+      for (auto& e : st_.pool)
+        if (!e->pinned && (w == nullptr || e->last_use < w->last_use))
+          w = e.get();
+    }
+    if (w == nullptr) {
+      auto e = std::make_unique<Workspace>();
+      if (cudaEventCreateWithFlags(&e->done, cudaEventDisableTiming) !=
+          cudaSuccess)
+        return SGEMM_ERR_CUDA;
+      e->stream = s_;
+      w = e.get();
+      st_.pool.push_back(std::move(e));
+    }
+    // Order this call after the workspace's previous call: a workspace
+    // handed over from another stream, or a stream handle that was
+    // destroyed and reissued with work of its old stream still running.
+    if (w->recorded && !cap &&
+        cudaStreamWaitEvent(s_, w->done, 0) != cudaSuccess)
+      return SGEMM_ERR_CUDA;
+    w->stream = s_;
+    w_ = w;
+    return SGEMM_OK;
+  }
+
+  DeviceState& st_;
+  cudaStream_t s_;
+  std::lock_guard<std::mutex> lock_;
+  Workspace* w_ = nullptr;
+};
+
+// Free `p` once the workspace's previous call is done (the host waits for
+// it; cudaFree itself may also wait for the device).
+void release(Workspace& w, void* p) {
+  if (p == nullptr) return;
+  if (w.recorded) cudaEventSynchronize(w.done);
+  cudaFree(p);
+}
+
+// Make the stream's workspace at least `floats` partial-tile floats and
+// `counters` tile counters. Growing replaces the buffer (cudaFree and
+// cudaMalloc: these may synchronise the device) and zeroes new counters
+// on the stream; the kernels leave the counters at zero when they finish.
+int ensure_workspace(Lease& ls, size_t floats, size_t counters,
+                     Workspace** out) {
+  Workspace* wp = nullptr;
+  const int rc = ls.get(&wp);
+  if (rc != SGEMM_OK) return rc;
+  Workspace& w = *wp;
   if (floats > w.ws_floats) {
-    if (w.ws != nullptr) cudaFree(w.ws);
+    release(w, w.ws);
     w.ws = nullptr;
     w.ws_floats = 0;
     if (cudaMalloc(&w.ws, floats * sizeof(float)) != cudaSuccess)
@@ -158,11 +262,12 @@ int ensure_workspace(DeviceState& st, cudaStream_t s, size_t floats,
     w.ws_floats = floats;
   }
   if (counters > w.counters_len) {
-    if (w.counters != nullptr) cudaFree(w.counters);
+    release(w, w.counters);
     w.counters = nullptr;
     w.counters_len = 0;
     if (cudaMalloc(&w.counters, counters * sizeof(int)) != cudaSuccess ||
-        cudaMemset(w.counters, 0, counters * sizeof(int)) != cudaSuccess)
+        cudaMemsetAsync(w.counters, 0, counters * sizeof(int),
+                        ls.stream()) != cudaSuccess)
       return SGEMM_ERR_CUDA;
     w.counters_len = counters;
   }
@@ -170,10 +275,15 @@ int ensure_workspace(DeviceState& st, cudaStream_t s, size_t floats,
   return SGEMM_OK;
 }
 
-// Grow the transposed-copy buffer of stream s's workspace (lock held).
-int ensure_tr(Workspace& w, size_t floats) {
+// Grow the transposed-copy buffer of the stream's workspace.
+int ensure_tr(Lease& ls, size_t floats, Workspace** out) {
+  Workspace* wp = nullptr;
+  const int rc = ls.get(&wp);
+  if (rc != SGEMM_OK) return rc;
+  Workspace& w = *wp;
+  *out = &w;
   if (floats <= w.tr_floats) return SGEMM_OK;
-  if (w.tr != nullptr) cudaFree(w.tr);
+  release(w, w.tr);
   w.tr = nullptr;
   w.tr_floats = 0;
   if (cudaMalloc(&w.tr, floats * sizeof(float)) != cudaSuccess)
@@ -372,9 +482,11 @@ int encode_tf32x3(const GemmArgs& g, CUtensorMap* tmA, CUtensorMap* tmB) {
                          sw);
 }
 
-// (st.ws_mu held: the pair kernel uses the stream's workspace.)
+// ls: the call's hold on its stream's workspace; nullptr when the call
+// may not allocate (then no split-k and the caller handles pairs).
 int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
-               bool pair, bool may_alloc = true) {
+               bool pair, Lease* ls) {
+  const bool may_alloc = ls != nullptr;
   CUtensorMap tmA, tmB;
   const int rc = encode_tf32x3(g, &tmA, &tmB);
   if (rc != SGEMM_OK) return rc;
@@ -386,7 +498,7 @@ int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
       return to_status(launch_tf32x3(g, tmA, tmB, st.status, s));
     Workspace* w = nullptr;
     const int wrc = ensure_workspace(
-        st, s, tf32x3_split_floats(g.M, g.N, g.batch, splits), 0, &w);
+        *ls, tf32x3_split_floats(g.M, g.N, g.batch, splits), 0, &w);
     if (wrc != SGEMM_OK) return wrc;
     return to_status(
         launch_tf32x3(g, tmA, tmB, st.status, s, splits, w->ws));
@@ -394,7 +506,8 @@ int run_tf32x3(const GemmArgs& g, DeviceState& st, cudaStream_t s,
   const PairPlan pl =
       plan_pair(g.M, g.N, g.K, st.pair_clusters, true, g.batch);
   Workspace* w = nullptr;
-  const int wrc = ensure_workspace(st, s, pl.ws_floats, pl.counters, &w);
+  if (ls == nullptr) return SGEMM_ERR_PATH;
+  const int wrc = ensure_workspace(*ls, pl.ws_floats, pl.counters, &w);
   if (wrc != SGEMM_OK) return wrc;
   // C by bulk tensor stores when it is not read (beta == 0) and aligned.
   // Rows must also end on a 16-byte boundary (N a multiple of 4): a bulk
@@ -513,15 +626,15 @@ int plan_path(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
 }
 
 // Replace transposed operands of g by row-major copies in the workspace of
-// stream s (st.ws_mu held): op(A) as M x K (ld K), op(B) as K x N (ld N).
-int make_row_major(GemmArgs& g, DeviceState& st, cudaStream_t s) {
+// the call's stream: op(A) as M x K (ld K), op(B) as K x N (ld N).
+int make_row_major(GemmArgs& g, Lease& ls) {
+  const cudaStream_t s = ls.stream();
   if (!g.op_a && !g.op_b) return SGEMM_OK;
   const size_t a_floats = g.op_a ? size_t(g.M) * size_t(g.K) : 0;
   const size_t a_pad = (a_floats + 63) / 64 * 64;  // B copy 256-byte aligned
   const size_t b_floats = g.op_b ? size_t(g.K) * size_t(g.N) : 0;
   Workspace* w = nullptr;
-  int rc = ensure_workspace(st, s, 0, 0, &w);
-  if (rc == SGEMM_OK) rc = ensure_tr(*w, a_pad + b_floats);
+  int rc = ensure_tr(ls, a_pad + b_floats, &w);
   if (rc != SGEMM_OK) return rc;
   if (g.op_a) {  // A stored K x M -> M x K
     rc = to_status(launch_transpose(g.A, g.lda, g.K, g.M, w->tr, s));
@@ -542,9 +655,10 @@ int make_row_major(GemmArgs& g, DeviceState& st, cudaStream_t s) {
 
 // Give the tensor maps operands they can take: each operand whose base or
 // row stride is not 16-byte aligned is copied (as stored, op unchanged)
-// into the workspace of stream s with its row stride rounded up to 4
-// floats (st.ws_mu held).
-int make_tensor_ready(GemmArgs& g, DeviceState& st, cudaStream_t s) {
+// into the workspace of the call's stream with its row stride rounded up to
+// 4 floats.
+int make_tensor_ready(GemmArgs& g, Lease& ls) {
+  const cudaStream_t s = ls.stream();
   const bool a_ok = tma_operand_ok(reinterpret_cast<uint64_t>(g.A), g.lda);
   const bool b_ok = tma_operand_ok(reinterpret_cast<uint64_t>(g.B), g.ldb);
   if (a_ok && b_ok) return SGEMM_OK;
@@ -554,8 +668,7 @@ int make_tensor_ready(GemmArgs& g, DeviceState& st, cudaStream_t s) {
   const size_t a_floats = a_ok ? 0 : (size_t(ar) * size_t(ald) + 63) / 64 * 64;
   const size_t b_floats = b_ok ? 0 : size_t(br) * size_t(bld);
   Workspace* w = nullptr;
-  int rc = ensure_workspace(st, s, 0, 0, &w);
-  if (rc == SGEMM_OK) rc = ensure_tr(*w, a_floats + b_floats);
+  int rc = ensure_tr(ls, a_floats + b_floats, &w);
   if (rc != SGEMM_OK) return rc;
   if (!a_ok) {
     rc = to_status(launch_repack(g.A, g.lda, ar, ac, w->tr, ald, s));
@@ -602,13 +715,13 @@ int run_call(const Call& call, void* stream, int path) {
   g.sc.beta = call.beta;
   g.op_a = call.op_a;
   g.op_b = call.op_b;
-  std::lock_guard<std::mutex> lock(st->ws_mu);  // workspace of stream s
+  Lease lease(*st, s);  // the workspace of stream s
   switch (path) {
     case SGEMM_PATH_TF32X3:
     case SGEMM_PATH_TF32X3_PAIR:
-      rc = make_tensor_ready(g, *st, s);
+      rc = make_tensor_ready(g, lease);
       if (rc != SGEMM_OK) return rc;
-      return run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR);
+      return run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR, &lease);
     case SGEMM_PATH_GEMV_COL: {
       if (call.M == 1 && call.N != 1 && call.op_b) {
         // c = op(a) * B^T: row j of B (stored N x K) times the vector a
@@ -623,7 +736,7 @@ int run_call(const Call& call, void* stream, int path) {
       if (g.op_a) {
         g.op_b = 0;  // B's column is read with its own stride below
         g.op_a = 1;
-        rc = make_row_major(g, *st, s);
+        rc = make_row_major(g, lease);
         if (rc != SGEMM_OK) return rc;
       }
       // the vector b = op(B)'s column: stride ldb (stored K x 1) or 1
@@ -642,13 +755,13 @@ int run_call(const Call& call, void* stream, int path) {
         return rc != SGEMM_OK ? rc : to_status(e);
       }
       if (call.M != 1) return SGEMM_ERR_PATH;
-      rc = make_row_major(g, *st, s);
+      rc = make_row_major(g, lease);
       if (rc != SGEMM_OK) return rc;
       const cudaError_t e = run_gemv_row(g, *st, s, &rc);
       return rc != SGEMM_OK ? rc : to_status(e);
     }
     case SGEMM_PATH_TILED_TMA: {
-      rc = make_row_major(g, *st, s);
+      rc = make_row_major(g, lease);
       if (rc != SGEMM_OK) return rc;
       if (!tma_operand_ok(reinterpret_cast<uint64_t>(g.A), g.lda) ||
           !tma_operand_ok(reinterpret_cast<uint64_t>(g.B), g.ldb))
@@ -661,17 +774,17 @@ int run_call(const Call& call, void* stream, int path) {
       const SkPlan pl =
           plan_stream_k(g.M, g.N, g.K, st->sms * st->tma_blocks_per_sm);
       Workspace* w = nullptr;
-      rc = ensure_workspace(*st, s, pl.ws_floats, size_t(pl.tiles), &w);
+      rc = ensure_workspace(lease, pl.ws_floats, size_t(pl.tiles), &w);
       if (rc != SGEMM_OK) return rc;
       return to_status(launch_tiled_tma(g, tmA, tmB, pl, w->ws, w->counters,
                                         st->status, s));
     }
     case SGEMM_PATH_TILED_LDG:
-      rc = make_row_major(g, *st, s);
+      rc = make_row_major(g, lease);
       if (rc != SGEMM_OK) return rc;
       return to_status(launch_tiled_ldg(g, st->status, s));
     case SGEMM_PATH_NAIVE:
-      rc = make_row_major(g, *st, s);
+      rc = make_row_major(g, lease);
       if (rc != SGEMM_OK) return rc;
       return to_status(launch_naive(g, s));
     default:
@@ -755,8 +868,10 @@ int run_batched(const Call& c, int64_t stride_a, int64_t stride_b,
     g.stride_b = stride_b;
     g.stride_c = stride_c;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(st->ws_mu);
-    rc = run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR);
+    {
+      Lease lease(*st, s);
+      rc = run_tf32x3(g, *st, s, path == SGEMM_PATH_TF32X3_PAIR, &lease);
+    }
     // a batch layout the tensor-map encoder refuses runs item by item
     if (rc != SGEMM_ERR_CUDA) return rc;
     path = SGEMM_PATH_AUTO;
@@ -821,7 +936,7 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
     case SGEMM_PATH_TF32X3:
-      return run_tf32x3(g, *st, s, false, false);
+      return run_tf32x3(g, *st, s, false, nullptr);
     case SGEMM_PATH_TF32X3_PAIR: {
       CUtensorMap tmA, tmB;
       rc = encode_tf32x3(g, &tmA, &tmB);
@@ -1092,13 +1207,25 @@ int sgemm_watchdog_status(int* site) {
   // raised; clear them so later calls start from zero.
   {
     std::lock_guard<std::mutex> lock(st->ws_mu);
-    for (auto& kv : st->ws)
-      if (kv.second.counters != nullptr &&
-          cudaMemset(kv.second.counters, 0,
-                     kv.second.counters_len * sizeof(int)) != cudaSuccess)
+    for (auto& w : st->pool)
+      if (w->counters != nullptr &&
+          cudaMemset(w->counters, 0, w->counters_len * sizeof(int)) !=
+              cudaSuccess)
         return SGEMM_ERR_CUDA;
   }
   return SGEMM_ERR_WATCHDOG;
+}
+
+int sgemm_workspace_info(int* count, int64_t* bytes) {
+  dfm::DeviceState* st = nullptr;
+  const int rc = dfm::device_state(&st);
+  if (rc != SGEMM_OK) return rc;
+  std::lock_guard<std::mutex> lock(st->ws_mu);
+  int64_t total = 0;
+  for (auto& w : st->pool) total += int64_t(w->bytes());
+  if (count != nullptr) *count = int(st->pool.size());
+  if (bytes != nullptr) *bytes = total;
+  return SGEMM_OK;
 }
 
 int sgemm_watchdog_selftest(void* stream, int64_t timeout_ns) {

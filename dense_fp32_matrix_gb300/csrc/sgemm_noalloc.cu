@@ -5,7 +5,7 @@
 // framework's caching pool or a fixed memory budget), code that must not
 // trigger the implicit device synchronisation of cudaMalloc/cudaFree in a
 // latency-critical loop, or plug-ins loaded into a host that forbids
-// allocation after start-up. sgemm() may grow its stream-K workspace with
+// allocation after start-up. sgemm() may grow its stream's workspace with
 // cudaMalloc on a call whose shape needs more; this entry point never does.
 //
 // How: the stream-K partial tiles and tile counters of the TMA path live in
@@ -27,14 +27,14 @@
 namespace dfm {
 namespace {
 
-// Largest stream-K grid the scratch serves (GB300 has 152 SMs; more
-// resident blocks are capped to this many).
+// Largest stream-K grid the scratch serves (GB300 has 152 SMs and the
+// kernel runs one block per SM; more resident blocks are capped to this).
 constexpr int kNoAllocMaxBlocks = 160;
-// Partial tiles: two 128 x 128 fp32 tiles per block (20 MiB).
+// Partial tiles: two 256 x 128 fp32 tiles per block (40 MiB).
 constexpr size_t kNoAllocPartialFloats =
     size_t(2) * kNoAllocMaxBlocks * kTileM * kTileN;
-// Tile counters: products with at most this many 128 x 128 output tiles
-// (for example M = N = 16384).
+// Tile counters: stream-K products with at most this many 256 x 128 output
+// tiles (for example M = 32768, N = 16384).
 constexpr size_t kNoAllocMaxTiles = 16384;
 constexpr size_t kNoAllocBytes =
     kNoAllocPartialFloats * sizeof(float) + kNoAllocMaxTiles * sizeof(int);
@@ -56,12 +56,9 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float* A,
                              int64_t lda, const float* B, int64_t ldb,
                              float* C, int64_t ldc, void* stream) {
   using namespace dfm;
-  if (M > 0 && N > 0) {
-    const int64_t tiles = ((M + kTileM - 1) / kTileM) *
-                          ((N + kTileN - 1) / kTileN);
-    if (tiles > int64_t(kNoAllocMaxTiles))
-      return SGEMM_ERR_TOO_LARGE;
-  }
+  // The tile limit applies where the scratch is used (the stream-K tile
+  // kernel): run_with_scratch rejects such a product before it enqueues
+  // anything; paths without scratch take any size sgemm takes.
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;

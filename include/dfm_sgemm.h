@@ -49,10 +49,28 @@
  *     stream). Every call is asynchronous on that stream; the library never
  *     synchronises. Errors found on the host are returned before anything is
  *     enqueued.
- *   - No entry point allocates device memory per call. The first call on a
- *     device does one-time set-up (device query, kernel attributes, the
- *     address of the per-device status word); make that first call outside
- *     any stream capture.
+ *   - Workspaces. Some paths need device memory beyond A, B and C: stream-K
+ *     partial tiles and tile counters, split-k pieces, row-major copies of
+ *     transposed operands for the CUDA-core kernels, and 16-byte-aligned
+ *     copies of misaligned operands for the tensor-core kernels. The library
+ *     keeps these in per-device workspaces, each serving one stream at a
+ *     time, at most 8 per device unless stream captures hold all 8
+ *     (sgemm_workspace_info reports them); they live until the process
+ *     exits. A call allocates only when its stream
+ *     has no workspace yet or needs a larger one: it then calls cudaMalloc,
+ *     and cudaFree for the outgrown buffer after waiting on the host for
+ *     that workspace's previous call, and these may synchronise the device.
+ *     A call whose needs fit its stream's workspace allocates nothing and
+ *     does not synchronise. With 8 workspaces in use, a ninth stream takes
+ *     the least recently used one, ordered after its last call by an event
+ *     wait on the device (no host synchronisation). A workspace used inside
+ *     a stream capture stays with its stream for good (the graph holds its
+ *     addresses). Make the first call of the largest shape on a stream
+ *     outside any capture: allocation is not allowed while capturing in the
+ *     global capture mode. sgemm_noalloc never allocates.
+ *   - The first call on a device does one-time set-up (device query, kernel
+ *     attributes, the address of the per-device status word); make that
+ *     first call outside any stream capture.
  *
  * Status codes: 0 on success, a negative SGEMM_ERR_* value otherwise;
  * sgemm_status_string() names each.
@@ -249,18 +267,25 @@ int sgemm_host(int64_t M, int64_t N, int64_t K, const float* hA, int64_t lda,
  * framework's caching pool, a fixed budget), latency-critical loops that
  * cannot afford the device-wide synchronisation cudaMalloc/cudaFree imply,
  * or plug-ins in hosts that forbid allocation after start-up. sgemm() may
- * grow its workspace with cudaMalloc; this entry point never calls
+ * grow its stream's workspace with cudaMalloc; this entry point never calls
  * cudaMalloc, cudaFree or any allocating routine. The pages have no
  * counterpart of this entry point.
  *
  * Scratch: the stream-K partial tiles and tile counters of the TMA path live
- * in one fixed device array of 20 MiB + 64 KiB that every device which loads
- * the library holds until the process exits. Limits: at most 16384 output
- * tiles of 128 x 128 (e.g. M = N = 16384); larger M x N returns
- * SGEMM_ERR_TOO_LARGE before any work is enqueued. The stream-K grid is
- * capped at 160 blocks. Operands whose base or row stride is not 16-byte
- * aligned take the any-layout CUDA-core tile kernel (sgemm would repack
- * them into allocated memory for the tensor path).
+ * in one fixed device array of 40 MiB + 64 KiB that every device which loads
+ * the library holds until the process exits. Limit: a product that takes
+ * the stream-K tile kernel (SGEMM_MATH_FFMA, aligned operands) may have at
+ * most 16384 output tiles of 256 x 128 (e.g. M = 32768, N = 16384); a
+ * larger one returns SGEMM_ERR_TOO_LARGE before any work is enqueued.
+ * (The pair kernel's pieces would need 38 MiB more, so it does not use
+ * the scratch.) Paths that use
+ * no scratch (the tensor-core kernels, the vector kernels, the any-layout
+ * tile kernel) take every size sgemm takes. The stream-K grid is capped at
+ * 160 blocks; the tensor-core pair kernel runs whole tiles only (its
+ * stream-K pieces would not fit) and the single-block tensor kernel does
+ * not split k. Operands whose base or row stride is not 16-byte aligned
+ * take the any-layout CUDA-core tile kernel (sgemm would repack them into
+ * allocated memory for the tensor path).
  *
  * The first call on a device fetches the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
@@ -294,6 +319,15 @@ int sgemm_watchdog_status(int* site);
  * SGEMM_ERR_WATCHDOG). Used to test failure detection without a GPU fault.
  */
 int sgemm_watchdog_selftest(void* stream, int64_t timeout_ns);
+
+/*
+ * sgemm_workspace_info: the workspaces the library holds on the current
+ * device: their number (*count) and their total size in bytes
+ * (*bytes). Either pointer may be NULL. Host only; returns SGEMM_OK, or
+ * the set-up errors of sgemm. No counterpart on the pages (a diagnostic of
+ * this library's memory use).
+ */
+int sgemm_workspace_info(int* count, int64_t* bytes);
 
 /* Human-readable name of a status code (static storage). */
 const char* sgemm_status_string(int status);

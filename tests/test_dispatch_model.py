@@ -43,7 +43,7 @@ def model(op_a, op_b, M, N, K, lda, ldb, ldc, a, b, math):
         return "tf32x3_pair" if pair else "tf32x3"
     a_ok = K % 4 == 0 if ta else tma_ok(a, lda)
     b_ok = N % 4 == 0 if tb else tma_ok(b, ldb)
-    iters = -(-M // 128) * -(-N // 128) * -(-K // 32)
+    iters = -(-M // 256) * -(-N // 128) * -(-K // 32)
     return "tiled_tma" if a_ok and b_ok and iters < (1 << 31) else "tiled_ldg"
 
 

@@ -10,8 +10,9 @@ import numpy as np
 import pytest
 
 import matgen
+import oracle
 from matgen.workloads import WORKLOADS
-from gpu_util import run_case
+from gpu_util import compare, run_case
 
 pytestmark = pytest.mark.gpu
 
@@ -260,9 +261,16 @@ def test_split_k_matches_unsplit_bitwise_on_integers():
     # integer data: every split and the single pass are exact, so equal
     import torch
     import dense_fp32_matrix_gb300 as dfm
-    A = torch.from_numpy(matgen.integers(12, 0, 512, 2048)).cuda()
-    B = torch.from_numpy(matgen.integers(12, 1, 2048, 384)).cuda()
+    A_h = matgen.integers(12, 0, 512, 2048)
+    B_h = matgen.integers(12, 1, 2048, 384)
+    A = torch.from_numpy(A_h).cuda()
+    B = torch.from_numpy(B_h).cuda()
     C = dfm.matmul(A, B, path=PATH)       # 12 tiles: split k
-    ref = (A.double() @ B.double()).float()
+    ref, S = oracle.gemm(A_h, B_h)
     torch.cuda.synchronize()
-    assert torch.equal(C, ref)
+    compare("integers", C.cpu().numpy(), ref, S, "split k")
+    # and another split of the same products (the pair kernel's stream-K
+    # schedule): exact sums, so the same bits
+    C1 = dfm.matmul(A, B, path=PAIR)
+    torch.cuda.synchronize()
+    assert torch.equal(C, C1)
