@@ -58,8 +58,9 @@ struct GemmArgs {
 
 // Tile geometry of the persistent TMA kernel (also used by the host
 // dispatcher). Block tile kTileM x kTileN, k-slices of kTileK, a
-// kTileStages-deep ring; kTileThreads threads, one block per SM; each lane
-// owns kLaneRows rows x (4 * kLaneChunks) columns of the block tile, with
+// kTileStages-deep ring; kTileThreads consumer threads (plus one producer
+// warpgroup that issues the copies), one block per SM; each lane owns
+// kLaneRows rows x (4 * kLaneChunks) columns of the block tile, with
 // kLanesN lanes of a warp along N.
 constexpr int kTileM = 256;
 constexpr int kTileN = 128;
@@ -83,13 +84,16 @@ struct SkPlan {
   int64_t total_iters = 0;
   int grid = 0;
   size_t ws_floats = 0;   // workspace: 2 partial tiles per block
+  size_t counters = 0;    // tile counters: kWarpsPerTile per tile
 };
+// The stream-K fix-up counts pieces per (tile, consumer warp).
+constexpr int kWarpsPerTile = kTileThreads / 32;
 SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K, int resident_blocks);
 
 // Main kernel with TMA loads. tmA / tmB must describe A (dims {K, M}, box
 // {kTileK, kTileM}, 128-byte swizzle) and B (dims {N, K}, box {kTileN,
 // kTileK}, no swizzle). ws holds pl.ws_floats floats; counters holds
-// pl.tiles ints, all zero (the kernel leaves them zero when it completes).
+// pl.counters ints, all zero (the kernel leaves them zero when it completes).
 cudaError_t launch_tiled_tma(const GemmArgs& g, const CUtensorMap& tmA,
                              const CUtensorMap& tmB, const SkPlan& pl,
                              float* ws, int* counters, int* status,

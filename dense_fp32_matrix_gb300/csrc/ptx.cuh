@@ -33,6 +33,7 @@ enum WaitSite : int {
   kSiteTf32Acc = 9,
   kSiteTf32Peer = 10,
   kSiteTf32Fix = 11,
+  kSiteTiledEmpty = 12,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -774,7 +774,7 @@ int run_call(const Call& call, void* stream, int path) {
       const SkPlan pl =
           plan_stream_k(g.M, g.N, g.K, st->sms * st->tma_blocks_per_sm);
       Workspace* w = nullptr;
-      rc = ensure_workspace(lease, pl.ws_floats, size_t(pl.tiles), &w);
+      rc = ensure_workspace(lease, pl.ws_floats, pl.counters, &w);
       if (rc != SGEMM_OK) return rc;
       return to_status(launch_tiled_tma(g, tmA, tmB, pl, w->ws, w->counters,
                                         st->status, s));
@@ -925,10 +925,10 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
       int resident = st->sms * st->tma_blocks_per_sm;
       if (resident > grid_cap) resident = grid_cap;
       const SkPlan pl = plan_stream_k(M, N, K, resident);
-      if (pl.ws_floats > ws_floats || size_t(pl.tiles) > counters_len)
+      if (pl.ws_floats > ws_floats || pl.counters > counters_len)
         return SGEMM_ERR_TOO_LARGE;
       rc = to_status(
-          cudaMemsetAsync(counters, 0, size_t(pl.tiles) * sizeof(int), s));
+          cudaMemsetAsync(counters, 0, pl.counters * sizeof(int), s));
       if (rc != SGEMM_OK) return rc;
       return to_status(
           launch_tiled_tma(g, tmA, tmB, pl, ws, counters, st->status, s));

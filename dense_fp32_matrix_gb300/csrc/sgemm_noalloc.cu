@@ -36,8 +36,10 @@ constexpr size_t kNoAllocPartialFloats =
 // Tile counters: stream-K products with at most this many 256 x 128 output
 // tiles (for example M = 32768, N = 16384).
 constexpr size_t kNoAllocMaxTiles = 16384;
+// The fix-up counts pieces per (tile, warp of the block).
+constexpr size_t kNoAllocCounters = kNoAllocMaxTiles * kWarpsPerTile;
 constexpr size_t kNoAllocBytes =
-    kNoAllocPartialFloats * sizeof(float) + kNoAllocMaxTiles * sizeof(int);
+    kNoAllocPartialFloats * sizeof(float) + kNoAllocCounters * sizeof(int);
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
@@ -73,6 +75,6 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float* A,
   int* counters = reinterpret_cast<int*>(
       sa.base + kNoAllocPartialFloats * sizeof(float));
   return run_with_scratch(M, N, K, A, lda, B, ldb, C, ldc, stream, partials,
-                          kNoAllocPartialFloats, counters, kNoAllocMaxTiles,
+                          kNoAllocPartialFloats, counters, kNoAllocCounters,
                           kNoAllocMaxBlocks);
 }

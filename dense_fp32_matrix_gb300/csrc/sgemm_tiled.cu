@@ -223,28 +223,42 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 // another block, so there is no co-residency requirement; the summation order
 // is fixed, so results are deterministic for a given shape and grid size.
 //
-// Stage hand-over: thread 0 issues the TMA loads, completion on one "full"
-// mbarrier per stage (the copies' transaction bytes). One block barrier per
-// k-slice, after the stage's copy has landed, tells thread 0 that every
-// warp has read the previous stage, which it then refills STAGES - 1
-// k-slices ahead. Measured at 4096^3, against this scheme: two hand-overs
-// without the block barrier, which let warps drift apart, were slower
-// (per-warp "stage empty" mbarriers that thread 0 waits on: 2.7 points of
-// the FMA peak; the last warp to finish a stage refilling it: 1.1
-// points), and so was an explicit shared->register double buffer of the
-// fragments (each row's next 4-k fragment loaded into the registers its
-// last use frees, the next B fragment during the current k: 0.5 points;
-// the compiler already schedules the unrolled slice's loads ahead).
+// Stage hand-over: a producer warpgroup issues the TMA copies (one thread
+// of it), completion on one "full" mbarrier per stage (the copies'
+// transaction bytes); the 256 consumer threads compute. Each consumer warp
+// arrives on the stage's "empty" mbarrier when it has read the stage; the
+// producer waits for all eight and refills the stage with the k-slice
+// STAGES later. No consumer waits for another (the warps drift apart by up
+// to the ring's depth) and the refill's work stays off the consumers' path.
+// setmaxnreg gives the consumers 232 registers and the producers 40
+// (2 x 128 x 232 + 128 x 40 = 384 threads x 168 at launch).
+// Measured at 4096^3 (% of the FP32 FMA peak at the sampled clock):
+//   * consumer thread 0 issuing the copies after one block barrier per
+//     k-slice: 77.2%; with the producer warpgroup and the consumers still
+//     passing a barrier per k-slice: 78.2%; without it (this scheme): 79.4%
+//     (80.5% at 8192^3);
+//   * without a producer warpgroup, letting warps drift was slower than the
+//     barrier: per-warp "stage empty" mbarriers that thread 0 waits on by
+//     2.7 points, the last warp to finish a stage refilling it by 1.1;
+//   * an explicit shared->register double buffer of the fragments (each
+//     row's next 4-k fragment loaded into the registers its last use
+//     frees, the next B fragment during the current k) was 0.5 points
+//     slower than the compiler's own scheduling of the unrolled slice, and
+//     an L2 prefetch of the boxes three k-slices beyond each copy changed
+//     nothing.
 
-// Producer state of the TMA copies, kept in shared memory: the next local
-// iteration to issue, its tile, k-slice and the tile's first row / column.
-struct Producer {
-  int v, tile, kt, m0, n0;
-};
+constexpr int TNT = TmaCfg::NT;                  // consumer threads
+constexpr int T_PRODUCER = 128;                  // the producer warpgroup
+constexpr int T_THREADS = TNT + T_PRODUCER;
+constexpr int kConsumerRegs = 232, kProducerRegs = 40;
+static_assert(TNT == 256, "two consumer warpgroups");
+static_assert(2 * 128 * kConsumerRegs + T_PRODUCER * kProducerRegs <=
+                  T_THREADS * 168,
+              "register split within the launch's 168 per thread");
 
-constexpr int TNT = TmaCfg::NT;
+
 constexpr size_t TMA_SMEM_BYTES =
-    size_t(TmaCfg::STAGES) * TmaCfg::STAGE_TX + 8 * TmaCfg::STAGES + 1024;
+    size_t(TmaCfg::STAGES) * TmaCfg::STAGE_TX + 16 * TmaCfg::STAGES + 1024;
 constexpr size_t LDG_SMEM_BYTES =
     size_t(LdgCfg::STAGES) * LdgCfg::STAGE_TX + 1024;
 
@@ -256,7 +270,7 @@ struct SkParams {
   int total_iters;         // T = tiles * I (< 2^31, checked by the host)
   int grid;                // G, with G <= T
   float* ws;               // 2 G partial tiles of BM x BN floats
-  int* counters;           // one per tile, zero between calls
+  int* counters;           // kWarpsPerTile per tile, zero between calls
   int vec_store;
   Scale sc;
   int* status;
@@ -296,27 +310,32 @@ __device__ __forceinline__ void add_partial(
     }
 }
 
-// Finish one partial segment of `tile` held in acc. my_slot: workspace slot
-// of this piece. Every piece, the last one included, goes through the
-// workspace, so the block that arrives last re-reads all pieces in piece
-// order and the sum does not depend on which block that is.
+// Finish one partial segment of `tile` held in acc, warp by warp: each
+// warp's share of a partial tile (its lanes' values) is separate, so each
+// warp stores its share of the piece, counts itself in on its own counter
+// (tile, warp) and, if it is the last of that warp position over the
+// tile's pieces, adds the pieces' shares in piece order (k order) and
+// writes its part of C. No warp waits for another, so warps that have
+// drifted apart by a few k-slices stay apart. Every piece, the last one
+// included, goes through the workspace, so the sum does not depend on
+// which block arrives last. my_slot: workspace slot of this piece.
 __device__ __forceinline__ void sk_fixup(
     const f2 (&acc)[TmaCfg::TM][TmaCfg::TJ], int tile, int my_slot,
-    const SkParams& p, float* C, int m0, int n0, int r0, int c0,
-    int* s_flag) {
+    const SkParams& p, float* C, int m0, int n0, int r0, int c0) {
   unsigned long long* ws = reinterpret_cast<unsigned long long*>(p.ws);
   constexpr int SLOT = TmaCfg::BM * TmaCfg::BN / 2;  // f2 values per tile
+  const int lane = threadIdx.x & 31;
+  int* counter = p.counters + tile * kWarpsPerTile + (threadIdx.x >> 5);
   store_partial(acc, ws + (long long)my_slot * SLOT);
   __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) *s_flag = atomicAdd(&p.counters[tile], 1);
-  __syncthreads();
+  __syncwarp();
+  int arrived = 0;
+  if (lane == 0) arrived = atomicAdd(counter, 1);
+  arrived = __shfl_sync(0xffffffffu, arrived, 0);
   const int x0 = tile * p.iters_per_tile;
   const int c_first = block_of(x0, p);
   const int c_last = block_of(x0 + p.iters_per_tile - 1, p);
   const int pieces = c_last - c_first + 1;
-  const int arrived = *s_flag;
-  __syncthreads();  // s_flag is reused by the next segment
   if (arrived != pieces - 1) return;
   __threadfence();
   f2 sum[TmaCfg::TM][TmaCfg::TJ];
@@ -330,7 +349,13 @@ __device__ __forceinline__ void sk_fixup(
   }
   store_tile<TmaCfg>(sum, C, p.M, p.N, p.ldc, m0, n0, r0, c0,
                      p.vec_store != 0, p.sc);
-  if (threadIdx.x == 0) p.counters[tile] = 0;
+  __syncwarp();
+  if (lane == 0) *counter = 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar)
+               : "memory");
 }
 
 // Bounded wait that also gives up at once when a thread of the block has
@@ -355,82 +380,79 @@ __device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity,
   return false;
 }
 
-__global__ void __launch_bounds__(TNT, 1)
+__global__ void __launch_bounds__(T_THREADS, 1)
 k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
             const __grid_constant__ CUtensorMap tmB, float* __restrict__ C,
             const SkParams p) {
   using Cf = TmaCfg;
   constexpr int STAGES = Cf::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_flag;
   __shared__ int s_abort;
-  __shared__ int s_issued[STAGES];  // last local iteration issued per slot
-  __shared__ Producer s_prod;
   uint8_t* smem = aligned_smem(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cf::A_STAGE;
   const uint32_t full0 = smem_u32(sB + STAGES * Cf::B_STAGE);
+  const uint32_t empty0 = full0 + 8 * STAGES;
   volatile int* abort_flag = &s_abort;
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
   const int I = p.iters_per_tile;
   const int it_begin = range_begin(blockIdx.x, p);
   const int it_end = range_begin(blockIdx.x + 1, p);
   const int n_local = it_end - it_begin;
-
-  // Issue the copies of the next local iteration into its slot and advance
-  // the producer state (thread 0 only; the tile's coordinates are
-  // recomputed only when the range moves to the next tile).
-  auto issue_next = [&]() {
-    Producer q = s_prod;
-    const int sl = q.v % STAGES;
-    const uint32_t bar = full0 + 8 * sl;
-    mbar_arrive_expect_tx(bar, Cf::STAGE_TX);
-    tma_load_2d(smem_u32(sA + sl * Cf::A_STAGE), &tmA, q.kt * Cf::BK, q.m0,
-                bar);
-    tma_load_2d(smem_u32(sB + sl * Cf::B_STAGE), &tmB, q.n0, q.kt * Cf::BK,
-                bar);
-    s_issued[sl] = q.v;
-    ++q.v;
-    if (++q.kt == I) {
-      q.kt = 0;
-      ++q.tile;
-      if (q.v < n_local) {  // the range continues in the next tile
-        int pm, pn;
-        tile_coords(q.tile, p.tiles_m, p.tiles_n, pm, pn);
-        q.m0 = pm * Cf::BM;
-        q.n0 = pn * Cf::BN;
-      }
-    }
-    s_prod = q;
-  };
 
   if (tid == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     for (int sl = 0; sl < STAGES; ++sl) {
       mbar_init(full0 + 8 * sl, 1);
-      s_issued[sl] = -1;
+      mbar_init(empty0 + 8 * sl, TNT / 32);  // one arrival per warp
     }
     mbar_fence_init();
     s_abort = 0;
-    Producer q;
-    q.v = 0;
-    q.tile = it_begin / I;
-    q.kt = it_begin - q.tile * I;
-    int pm, pn;
-    tile_coords(q.tile, p.tiles_m, p.tiles_n, pm, pn);
-    q.m0 = pm * Cf::BM;
-    q.n0 = pn * Cf::BN;
-    s_prod = q;
-    for (int v = 0; v < STAGES - 1 && v < n_local; ++v) issue_next();
   }
-  __syncthreads();
+  __syncthreads();  // the last barrier the producer warpgroup joins
 
+  if (tid >= TNT) {
+    // ---- producer warpgroup: one thread issues the copies.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    if (tid != TNT) return;
+    int tile = it_begin / I, kt = it_begin - tile * I, pm, pn;
+    tile_coords(tile, p.tiles_m, p.tiles_n, pm, pn);
+    int issued = 0;
+    for (int v = 0; v < n_local; ++v) {
+      const int sl = v % STAGES;
+      // use v / STAGES - 1 of the slot (local iteration v - STAGES) read
+      if (v >= STAGES &&
+          !wait_stage(empty0 + 8 * sl, uint32_t(v / STAGES - 1) & 1u,
+                      abort_flag, p.status, kSiteTiledEmpty))
+        break;
+      if (*abort_flag != 0) break;
+      const uint32_t bar = full0 + 8 * sl;
+      mbar_arrive_expect_tx(bar, Cf::STAGE_TX);
+      tma_load_2d(smem_u32(sA + sl * Cf::A_STAGE), &tmA, kt * Cf::BK,
+                  pm * Cf::BM, bar);
+      tma_load_2d(smem_u32(sB + sl * Cf::B_STAGE), &tmB, pn * Cf::BN,
+                  kt * Cf::BK, bar);
+      issued = v + 1;
+      if (++kt == I && v + 1 < n_local) {  // the range goes on to the next tile
+        kt = 0;
+        tile_coords(++tile, p.tiles_m, p.tiles_n, pm, pn);
+      }
+    }
+    // The block's shared memory lives until this thread exits: let the
+    // last copy of each slot land (at once unless the block aborted).
+    for (int v = issued - STAGES > 0 ? issued - STAGES : 0; v < issued; ++v)
+      mbar_wait_bounded(full0 + 8 * (v % STAGES), uint32_t(v / STAGES) & 1u,
+                        nullptr, kSiteTiledDrain, kWaitLimitNs / 100);
+    return;
+  }
+
+  // ---- consumers
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
   f2 acc[Cf::TM][Cf::TJ];
   zero_acc<Cf>(acc);
 
-  const int lane_m = lane / Cf::LANES_N;
+  const int lane_m = (tid & 31) / Cf::LANES_N;
   const int r0 = lane_row0<Cf>(tid), c0 = lane_col0<Cf>(tid);
   const uint8_t* a_rows = sA + r0 * Cf::A_ROW;
   const uint8_t* b_cols = sB + c0 * 4;
@@ -441,15 +463,13 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
     const int it = it_begin + u;
     const bool landed = wait_stage(full0 + 8 * slot, phase, abort_flag,
                                    p.status, kSiteTiledFull);
-    // Every thread has finished local iteration u - 1 (its stage may be
-    // refilled, STAGES - 1 k-slices ahead) and the block takes one decision
-    // on an abort.
-    const bool skip = __syncthreads_or(!landed);
-    if (!skip) {
-      if (tid == 0 && u + STAGES - 1 < n_local) issue_next();
+    if (__all_sync(0xffffffffu, landed))
       compute_slice<Cf>(acc, a_rows + slot * Cf::A_STAGE,
                         b_cols + slot * Cf::B_STAGE, lane_m);
-    }
+    // this warp is done with the stage: once all eight are, the producer
+    // refills it with local iteration u + STAGES
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(empty0 + 8 * slot);
     if (++slot == STAGES) {
       slot = 0;
       phase ^= 1u;
@@ -465,20 +485,9 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
                        c0, p.vec_store != 0, p.sc);
       else
         sk_fixup(acc, tile, 2 * blockIdx.x + (it_begin >= tile_begin ? 0 : 1),
-                 p, C, pm * Cf::BM, pn * Cf::BN, r0, c0, &s_flag);
+                 p, C, pm * Cf::BM, pn * Cf::BN, r0, c0);
       zero_acc<Cf>(acc);
       tile_end += I;
-    }
-  }
-  __syncthreads();  // no copy is issued after this point
-  if (tid == 0 && *abort_flag != 0) {
-    // Let this block's copies land (bounded) before its shared memory is
-    // released: the last copy of each slot, if it is still in flight.
-    for (int sl = 0; sl < STAGES; ++sl) {
-      const int v = s_issued[sl];
-      if (v >= 0)
-        mbar_wait_bounded(full0 + 8 * sl, uint32_t(v / STAGES) & 1u, nullptr,
-                          kSiteTiledDrain, kWaitLimitNs / 100);
     }
   }
 }
@@ -585,7 +594,7 @@ cudaError_t tiled_init(int* tma_blocks_per_sm) {
                            int(LDG_SMEM_BYTES));
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      tma_blocks_per_sm, k_tiled_tma, TNT, TMA_SMEM_BYTES);
+      tma_blocks_per_sm, k_tiled_tma, T_THREADS, TMA_SMEM_BYTES);
 }
 
 SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K, int resident_blocks) {
@@ -597,6 +606,7 @@ SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K, int resident_blocks) {
                                              : int(pl.total_iters);
   if (pl.grid < 1) pl.grid = 1;
   pl.ws_floats = size_t(2) * pl.grid * kTileM * kTileN;
+  pl.counters = size_t(pl.tiles) * kWarpsPerTile;
   return pl;
 }
 
@@ -619,7 +629,7 @@ cudaError_t launch_tiled_tma(const GemmArgs& g, const CUtensorMap& tmA,
   p.vec_store = vec_ok(g) ? 1 : 0;
   p.sc = g.sc;
   p.status = status;
-  k_tiled_tma<<<pl.grid, TNT, TMA_SMEM_BYTES, s>>>(tmA, tmB, g.C, p);
+  k_tiled_tma<<<pl.grid, T_THREADS, TMA_SMEM_BYTES, s>>>(tmA, tmB, g.C, p);
   return cudaGetLastError();
 }
 

@@ -272,7 +272,7 @@ int sgemm_host(int64_t M, int64_t N, int64_t K, const float* hA, int64_t lda,
  * counterpart of this entry point.
  *
  * Scratch: the stream-K partial tiles and tile counters of the TMA path live
- * in one fixed device array of 40 MiB + 64 KiB that every device which loads
+ * in one fixed device array of 40 MiB + 512 KiB that every device which loads
  * the library holds until the process exits. Limit: a product that takes
  * the stream-K tile kernel (SGEMM_MATH_FFMA, aligned operands) may have at
  * most 16384 output tiles of 256 x 128 (e.g. M = 32768, N = 16384); a
