@@ -76,16 +76,21 @@ constexpr int kLanesN = 8;
 cudaError_t tiled_init(int* tma_blocks_per_sm);
 cudaError_t small_init();
 
-// Stream-K schedule of the TMA tile kernel: G = min(resident blocks, T)
-// persistent blocks share T = tiles x iters_per_tile k-slice iterations.
+// Schedule of the TMA tile kernel: G = min(resident blocks, T) persistent
+// blocks over T = tiles x iters_per_tile k-slices: whole tiles in full
+// waves, the k-slices of the other tiles split evenly (stream-K).
 struct SkPlan {
   int64_t tiles = 0;
   int64_t iters_per_tile = 0;
   int64_t total_iters = 0;
   int grid = 0;
+  int64_t dp_tiles = 0;   // tiles dealt whole in full waves
+  int64_t sk_iters = 0;   // k-slices of the other tiles, split evenly
   size_t ws_floats = 0;   // workspace: 2 partial tiles per block
-  size_t counters = 0;    // tile counters: kWarpsPerTile per tile
+  size_t counters = 0;    // kWarpsPerTile per split tile
 };
+// Smallest share of split k-slices per block worth a fix-up.
+constexpr int64_t kMinSkShare = 8;
 // The stream-K fix-up counts pieces per (tile, consumer warp).
 constexpr int kWarpsPerTile = kTileThreads / 32;
 SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K, int resident_blocks);
@@ -189,7 +194,9 @@ namespace dfm {
 // C = A * B like sgemm, but the stream-K TMA path takes its partial tiles
 // and tile counters from caller-provided device scratch (ws: ws_floats
 // floats, counters: counters_len ints) with at most grid_cap blocks, and no
-// device memory is allocated. The counters used are cleared on the stream
+// device memory is allocated. That path refuses products of more than
+// counters_len / kWarpsPerTile tiles (SGEMM_ERR_TOO_LARGE, nothing
+// enqueued). The counters used are cleared on the stream
 // before the launch. Returns an SGEMM_* status.
 int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
                      int64_t lda, const float* B, int64_t ldb, float* C,

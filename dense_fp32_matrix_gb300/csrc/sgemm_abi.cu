@@ -925,7 +925,11 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
       int resident = st->sms * st->tma_blocks_per_sm;
       if (resident > grid_cap) resident = grid_cap;
       const SkPlan pl = plan_stream_k(M, N, K, resident);
-      if (pl.ws_floats > ws_floats || pl.counters > counters_len)
+      // The documented limit: counters for every tile (whatever part of
+      // them this schedule splits), before anything is enqueued.
+      if (pl.ws_floats > ws_floats ||
+          size_t(pl.tiles) * kWarpsPerTile > counters_len ||
+          pl.counters > counters_len)
         return SGEMM_ERR_TOO_LARGE;
       rc = to_status(
           cudaMemsetAsync(counters, 0, pl.counters * sizeof(int), s));

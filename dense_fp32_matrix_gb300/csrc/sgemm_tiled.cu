@@ -267,24 +267,26 @@ struct SkParams {
   long long ldc;
   int tiles_m, tiles_n;
   int iters_per_tile;      // I
-  int total_iters;         // T = tiles * I (< 2^31, checked by the host)
-  int grid;                // G, with G <= T
+  int grid;                // G
+  int dp_tiles;            // tiles dealt whole, tile t to block t mod G
+  int sk_iters;            // k-slices of the other tiles, split evenly
   float* ws;               // 2 G partial tiles of BM x BN floats
-  int* counters;           // kWarpsPerTile per tile, zero between calls
+  int* counters;           // kWarpsPerTile per split tile, zero between calls
   int vec_store;
   Scale sc;
   int* status;
 };
 
+// Start of block c's share of the split k-slices (the T = sk_iters
+// k-slices of the tiles past dp_tiles, laid out tile by tile).
 __device__ __forceinline__ int range_begin(int c, const SkParams& p) {
-  return int((long long)c * p.total_iters / p.grid);
+  return int((long long)c * p.sk_iters / p.grid);
 }
 
 // Index of the block whose range holds iteration x: the largest c with
 // floor(c T / G) <= x.
 __device__ __forceinline__ int block_of(int x, const SkParams& p) {
-  return int(((long long)(x + 1) * p.grid + p.total_iters - 1) /
-             p.total_iters) - 1;
+  return int(((long long)(x + 1) * p.grid + p.sk_iters - 1) / p.sk_iters) - 1;
 }
 
 // Partial tiles are stored thread-major: value q of thread t at q * NT + t,
@@ -325,14 +327,15 @@ __device__ __forceinline__ void sk_fixup(
   unsigned long long* ws = reinterpret_cast<unsigned long long*>(p.ws);
   constexpr int SLOT = TmaCfg::BM * TmaCfg::BN / 2;  // f2 values per tile
   const int lane = threadIdx.x & 31;
-  int* counter = p.counters + tile * kWarpsPerTile + (threadIdx.x >> 5);
+  const int sk_tile = tile - p.dp_tiles;
+  int* counter = p.counters + sk_tile * kWarpsPerTile + (threadIdx.x >> 5);
   store_partial(acc, ws + (long long)my_slot * SLOT);
   __threadfence();
   __syncwarp();
   int arrived = 0;
   if (lane == 0) arrived = atomicAdd(counter, 1);
   arrived = __shfl_sync(0xffffffffu, arrived, 0);
-  const int x0 = tile * p.iters_per_tile;
+  const int x0 = sk_tile * p.iters_per_tile;
   const int c_first = block_of(x0, p);
   const int c_last = block_of(x0 + p.iters_per_tile - 1, p);
   const int pieces = c_last - c_first + 1;
@@ -380,6 +383,51 @@ __device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// A block's work as a run of segments, each a k-range of one tile: first
+// its share of the split k-slices (tile by tile, a partial segment at
+// either end), then its whole tiles (b, b + G, ... below dp_tiles). The
+// producer and the consumers walk the same sequence.
+struct Segments {
+  int x, x_end;  // next split k-slice, end of the share
+  int dp_next;   // next whole tile
+};
+struct Segment {
+  int tile, kt0, len;
+  bool whole;
+};
+
+__device__ __forceinline__ Segments block_segments(const SkParams& p) {
+  Segments sg;
+  sg.x = range_begin(blockIdx.x, p);
+  sg.x_end = range_begin(blockIdx.x + 1, p);
+  sg.dp_next = blockIdx.x;
+  return sg;
+}
+
+__device__ __forceinline__ bool next_segment(Segments& sg, const SkParams& p,
+                                             Segment& g) {
+  const int I = p.iters_per_tile;
+  if (sg.x < sg.x_end) {
+    const int t = sg.x / I;
+    const int end = min(sg.x_end, (t + 1) * I);
+    g.tile = p.dp_tiles + t;
+    g.kt0 = sg.x - t * I;
+    g.len = end - sg.x;
+    g.whole = g.kt0 == 0 && g.len == I;
+    sg.x = end;
+    return true;
+  }
+  if (sg.dp_next < p.dp_tiles) {
+    g.tile = sg.dp_next;
+    g.kt0 = 0;
+    g.len = I;
+    g.whole = true;
+    sg.dp_next += p.grid;
+    return true;
+  }
+  return false;
+}
+
 __global__ void __launch_bounds__(T_THREADS, 1)
 k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
             const __grid_constant__ CUtensorMap tmB, float* __restrict__ C,
@@ -395,10 +443,6 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
   const uint32_t empty0 = full0 + 8 * STAGES;
   volatile int* abort_flag = &s_abort;
   const int tid = threadIdx.x;
-  const int I = p.iters_per_tile;
-  const int it_begin = range_begin(blockIdx.x, p);
-  const int it_end = range_begin(blockIdx.x + 1, p);
-  const int n_local = it_end - it_begin;
 
   if (tid == 0) {
     tma_prefetch_desc(&tmA);
@@ -416,27 +460,30 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
     // ---- producer warpgroup: one thread issues the copies.
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (tid != TNT) return;
-    int tile = it_begin / I, kt = it_begin - tile * I, pm, pn;
-    tile_coords(tile, p.tiles_m, p.tiles_n, pm, pn);
-    int issued = 0;
-    for (int v = 0; v < n_local; ++v) {
-      const int sl = v % STAGES;
-      // use v / STAGES - 1 of the slot (local iteration v - STAGES) read
-      if (v >= STAGES &&
-          !wait_stage(empty0 + 8 * sl, uint32_t(v / STAGES - 1) & 1u,
-                      abort_flag, p.status, kSiteTiledEmpty))
-        break;
-      if (*abort_flag != 0) break;
-      const uint32_t bar = full0 + 8 * sl;
-      mbar_arrive_expect_tx(bar, Cf::STAGE_TX);
-      tma_load_2d(smem_u32(sA + sl * Cf::A_STAGE), &tmA, kt * Cf::BK,
-                  pm * Cf::BM, bar);
-      tma_load_2d(smem_u32(sB + sl * Cf::B_STAGE), &tmB, pn * Cf::BN,
-                  kt * Cf::BK, bar);
-      issued = v + 1;
-      if (++kt == I && v + 1 < n_local) {  // the range goes on to the next tile
-        kt = 0;
-        tile_coords(++tile, p.tiles_m, p.tiles_n, pm, pn);
+    Segments sg = block_segments(p);
+    Segment g;
+    int issued = 0;  // local k-slices issued
+    bool stop = false;
+    while (!stop && next_segment(sg, p, g)) {
+      int pm, pn;
+      tile_coords(g.tile, p.tiles_m, p.tiles_n, pm, pn);
+      for (int s = 0; s < g.len; ++s) {
+        const int v = issued, sl = v % STAGES;
+        // use v / STAGES - 1 of the slot (local k-slice v - STAGES) read
+        if ((v >= STAGES &&
+             !wait_stage(empty0 + 8 * sl, uint32_t(v / STAGES - 1) & 1u,
+                         abort_flag, p.status, kSiteTiledEmpty)) ||
+            *abort_flag != 0) {
+          stop = true;
+          break;
+        }
+        const uint32_t bar = full0 + 8 * sl;
+        mbar_arrive_expect_tx(bar, Cf::STAGE_TX);
+        tma_load_2d(smem_u32(sA + sl * Cf::A_STAGE), &tmA,
+                    (g.kt0 + s) * Cf::BK, pm * Cf::BM, bar);
+        tma_load_2d(smem_u32(sB + sl * Cf::B_STAGE), &tmB, pn * Cf::BN,
+                    (g.kt0 + s) * Cf::BK, bar);
+        issued = v + 1;
       }
     }
     // The block's shared memory lives until this thread exits: let the
@@ -458,37 +505,33 @@ k_tiled_tma(const __grid_constant__ CUtensorMap tmA,
   const uint8_t* b_cols = sB + c0 * 4;
   int slot = 0;
   uint32_t phase = 0;
-  int tile_end = (it_begin / I + 1) * I;  // end of the current tile's slices
-  for (int u = 0; u < n_local; ++u) {
-    const int it = it_begin + u;
-    const bool landed = wait_stage(full0 + 8 * slot, phase, abort_flag,
-                                   p.status, kSiteTiledFull);
-    if (__all_sync(0xffffffffu, landed))
-      compute_slice<Cf>(acc, a_rows + slot * Cf::A_STAGE,
-                        b_cols + slot * Cf::B_STAGE, lane_m);
-    // this warp is done with the stage: once all eight are, the producer
-    // refills it with local iteration u + STAGES
-    __syncwarp();
-    if ((tid & 31) == 0) mbar_arrive(empty0 + 8 * slot);
-    if (++slot == STAGES) {
-      slot = 0;
-      phase ^= 1u;
+  Segments sg = block_segments(p);
+  Segment g;
+  for (int seg = 0; next_segment(sg, p, g); ++seg) {
+    for (int s = 0; s < g.len; ++s) {
+      const bool landed = wait_stage(full0 + 8 * slot, phase, abort_flag,
+                                     p.status, kSiteTiledFull);
+      if (__all_sync(0xffffffffu, landed))
+        compute_slice<Cf>(acc, a_rows + slot * Cf::A_STAGE,
+                          b_cols + slot * Cf::B_STAGE, lane_m);
+      // this warp is done with the stage: once all eight are, the
+      // producer refills it with the k-slice STAGES later
+      __syncwarp();
+      if ((tid & 31) == 0) mbar_arrive(empty0 + 8 * slot);
+      if (++slot == STAGES) {
+        slot = 0;
+        phase ^= 1u;
+      }
     }
-    if (it + 1 == it_end || it + 1 == tile_end) {
-      // End of a segment: [max(it_begin, tile start), it] of one tile.
-      const int tile = tile_end / I - 1;
-      const int tile_begin = tile_end - I;
-      int pm, pn;
-      tile_coords(tile, p.tiles_m, p.tiles_n, pm, pn);
-      if (it_begin <= tile_begin && it + 1 == tile_end)
-        store_tile<Cf>(acc, C, p.M, p.N, p.ldc, pm * Cf::BM, pn * Cf::BN, r0,
-                       c0, p.vec_store != 0, p.sc);
-      else
-        sk_fixup(acc, tile, 2 * blockIdx.x + (it_begin >= tile_begin ? 0 : 1),
-                 p, C, pm * Cf::BM, pn * Cf::BN, r0, c0);
-      zero_acc<Cf>(acc);
-      tile_end += I;
-    }
+    int pm, pn;
+    tile_coords(g.tile, p.tiles_m, p.tiles_n, pm, pn);
+    if (g.whole)
+      store_tile<Cf>(acc, C, p.M, p.N, p.ldc, pm * Cf::BM, pn * Cf::BN, r0,
+                     c0, p.vec_store != 0, p.sc);
+    else  // the first segment of a share is piece 0, its last one piece 1
+      sk_fixup(acc, g.tile, 2 * blockIdx.x + (seg == 0 ? 0 : 1), p, C,
+               pm * Cf::BM, pn * Cf::BN, r0, c0);
+    zero_acc<Cf>(acc);
   }
 }
 
@@ -605,8 +648,18 @@ SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K, int resident_blocks) {
   pl.grid = resident_blocks < pl.total_iters ? resident_blocks
                                              : int(pl.total_iters);
   if (pl.grid < 1) pl.grid = 1;
+  // Whole tiles in full waves; the k-slices of the remaining tiles split
+  // evenly over all blocks. A share under kMinSkShare k-slices would cut
+  // each of those tiles into many small pieces: one more wave is split.
+  int64_t waves = pl.tiles / pl.grid;
+  const int64_t rest = pl.tiles - waves * pl.grid;
+  if (waves > 0 && rest > 0 &&
+      rest * pl.iters_per_tile < kMinSkShare * int64_t(pl.grid))
+    --waves;
+  pl.dp_tiles = waves * pl.grid;
+  pl.sk_iters = (pl.tiles - pl.dp_tiles) * pl.iters_per_tile;
   pl.ws_floats = size_t(2) * pl.grid * kTileM * kTileN;
-  pl.counters = size_t(pl.tiles) * kWarpsPerTile;
+  pl.counters = size_t(pl.tiles - pl.dp_tiles) * kWarpsPerTile;
   return pl;
 }
 
@@ -622,7 +675,8 @@ cudaError_t launch_tiled_tma(const GemmArgs& g, const CUtensorMap& tmA,
   p.tiles_m = int((g.M + kTileM - 1) / kTileM);
   p.tiles_n = int((g.N + kTileN - 1) / kTileN);
   p.iters_per_tile = int(pl.iters_per_tile);
-  p.total_iters = int(pl.total_iters);
+  p.dp_tiles = int(pl.dp_tiles);
+  p.sk_iters = int(pl.sk_iters);
   p.grid = pl.grid;
   p.ws = ws;
   p.counters = counters;

@@ -108,16 +108,23 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
     # In the CUDA-core mode an aligned product takes the stream-K kernel,
     # whose tile counters live in the scratch: 16385 output tiles of
     # 256 x 128 is one over the limit, rejected on the host before anything
-    # is enqueued (the pointers are never touched).
+    # is enqueued. The buffers are real (2.1 GB for C) and C is checked
+    # untouched, so a regression shows up as a failed assertion.
+    import torch
+    M, N, K = 256 * 16385, 128, 4
+    A = torch.zeros((M, K), device="cuda")
+    B = torch.zeros((K, N), device="cuda")
+    C = torch.full((M, N), 7.0, device="cuda")
+    torch.cuda.synchronize()
     previous = lib.sgemm_set_math_mode(1)
     try:
-        M, N = 256 * 16385, 128
-        fake = 1 << 40
-        rc = lib.sgemm_noalloc(M, N, 4, fake, 4, fake + (1 << 36), N,
-                               fake + (1 << 38), N, None)
+        rc = lib.sgemm_noalloc(M, N, K, A.data_ptr(), K, B.data_ptr(), N,
+                               C.data_ptr(), N, None)
     finally:
         lib.sgemm_set_math_mode(previous)
+    torch.cuda.synchronize()
     assert rc == TOO_LARGE
+    assert bool((C[::4096] == 7.0).all())
 
 
 def test_noalloc_limit_spares_paths_without_scratch(lib):
