@@ -395,14 +395,35 @@ def run_gpu(args, w):
     A = torch.from_numpy(matgen.KINDS[w["kind"]](w["seed"], 0, M, K)).cuda()
     B = torch.from_numpy(matgen.KINDS[w["kind"]](w["seed"], 1, K, N)).cuda()
     C = torch.empty((M, N), device="cuda")
+    # Layout of the timed product: dense by default; --pad adds floats to
+    # every row of A, B and C (leading dimensions K + pad, N + pad) and
+    # --offset shifts their bases by that many floats (misaligned for the
+    # paths that need 16-byte rows). A, B, C keep dense copies for the e2e
+    # leg and its check.
+    lda, ldb, ldc = K + args.pad, N + args.pad, N + args.pad
+    keep = []
+
+    def placed(X, rows, cols, ld):
+        buf = torch.zeros(args.offset + rows * ld + 4, device="cuda")
+        buf[args.offset:args.offset + rows * ld].view(rows, ld)[:, :cols] = X
+        keep.append(buf)
+        view = buf[args.offset:args.offset + rows * ld].view(rows, ld)[:, :cols]
+        return buf.data_ptr() + 4 * args.offset, view
+
+    if args.pad or args.offset:
+        pA, _ = placed(A, M, K, lda)
+        pB, _ = placed(B, K, N, ldb)
+        pC, C = placed(C, M, N, ldc)
+    else:
+        pA, pB, pC = A.data_ptr(), B.data_ptr(), C.data_ptr()
     flush = L2Flush()
     stream = torch.cuda.current_stream()
     path_name = args.path
-    plan = dfm.sgemm_plan(M, N, K, K, N, N, A.data_ptr(), B.data_ptr(),
-                          C.data_ptr()) if path_name == "auto" else path_name
+    plan = dfm.sgemm_plan(M, N, K, lda, ldb, ldc, pA, pB,
+                          pC) if path_name == "auto" else path_name
 
     def step():
-        dfm.sgemm_path(M, N, K, A, K, B, N, C, N, stream, path_name)
+        dfm.sgemm_path(M, N, K, pA, lda, pB, ldb, pC, ldc, stream, path_name)
 
     for _ in range(args.warmup):
         flush()
@@ -443,15 +464,15 @@ def run_gpu(args, w):
     hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
     dA = torch.empty_like(A)
     dB = torch.empty_like(B)
-    dC = torch.empty_like(C)
+    dC = torch.empty((M, N), device="cuda")
     e2e_steps = max(3, min(args.steps, 50))
     # sgemm_host takes sgemm's own path choice; with a forced CUDA-core path
     # the e2e leg runs in the CUDA-core math mode so that it computes with
     # the same arithmetic.
     prev_mode = dfm.sgemm_set_math_mode(
         "auto" if plan.startswith("tf32x3") else "ffma")
-    e2e_plan = dfm.sgemm_plan(M, N, K, K, N, N, A.data_ptr(), B.data_ptr(),
-                              C.data_ptr())
+    e2e_plan = dfm.sgemm_plan(M, N, K, K, N, N, dA.data_ptr(),
+                              dB.data_ptr(), dC.data_ptr())
     for _ in range(3):
         dfm.sgemm_host(M, N, K, hA, K, hB, N, hC, N, dA, dB, dC, stream)
     torch.cuda.synchronize()
@@ -485,8 +506,8 @@ def run_gpu(args, w):
     clock_mhz = clk["sm_mhz"] or (clk["sm_max_mhz"] or 2070.0)
     kernel = {"tiled_tma": "k_tiled_tma", "tiled_ldg": "k_tiled_ldg",
               "tf32x3": "k_tf32x3", "tf32x3_pair": "k_tf32x3_pair",
-              "gemv_row": "k_gemv_row_tma", "gemv_col": "k_gemv_col_tma"}.get(
-                  plan, plan)
+              "gemv_row": "k_gemv_row_tma", "gemv_col": "k_gemv_col_tma",
+              "small": "k_small", "naive": "k_naive"}.get(plan, plan)
     if plan.startswith("tf32x3"):
         # Roofline of the tensor kernels: the dense TF32 rate of the tensor
         # cores at the SM clock of the timed region (ncu's per-clock rate of
@@ -545,8 +566,7 @@ def run_gpu(args, w):
     if plan.startswith("tf32x3") and not args.no_ffma:
         prev = dfm.sgemm_set_math_mode("ffma")
         try:
-            ffma_path = dfm.sgemm_plan(M, N, K, K, N, N, A.data_ptr(),
-                                       B.data_ptr(), C.data_ptr())
+            ffma_path = dfm.sgemm_plan(M, N, K, lda, ldb, ldc, pA, pB, pC)
             with ClockSampler(dev) as fclocks:
                 fms = time_steps(step, flush, stream,
                                  max(5, min(args.steps, 100)), args.warmup,
@@ -592,7 +612,12 @@ def run_gpu(args, w):
             "l2": "flushed before every step (a 256 MiB device write, then "
                   "a 256 MiB read so no dirty lines remain; outside the timed "
                   "events)",
-            "parallelism": "replicas" if world > 1 else "single GPU"}),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "layout": ("row-major, dense leading dimensions"
+                       if not (args.pad or args.offset) else
+                       "row-major, lda = K + %d, ldb = ldc = N + %d, bases "
+                       "shifted by %d floats" % (args.pad, args.pad,
+                                                 args.offset))}),
         "roofline": roof,
         "ffma_kernel": ffma,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_mhz_min": clk.get("sm_mhz_min"),
@@ -640,6 +665,11 @@ def main(argv=None):
     p.add_argument("--path", default="auto",
                    help="force a kernel path (auto, tiled_tma, tiled_ldg, ...)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--pad", type=int, default=0,
+                   help="extra floats per row of A, B and C (leading "
+                        "dimensions K + pad, N + pad)")
+    p.add_argument("--offset", type=int, default=0,
+                   help="shift the bases of A, B and C by this many floats")
     p.add_argument("--no-ffma", action="store_true",
                    help="skip timing the CUDA-core kernel beside the tensor one")
     args = p.parse_args(argv)

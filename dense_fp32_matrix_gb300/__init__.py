@@ -28,7 +28,8 @@ STATUS = {
 }
 MATH = {"auto": 0, "ffma": 1}
 PATHS = {"auto": 0, "tiled_tma": 1, "tiled_ldg": 2, "gemv_row": 3,
-         "gemv_col": 4, "naive": 5, "tf32x3": 6, "tf32x3_pair": 7}
+         "gemv_col": 4, "naive": 5, "tf32x3": 6, "tf32x3_pair": 7,
+         "small": 8}
 
 
 class SgemmError(RuntimeError):

@@ -172,6 +172,10 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
 cudaError_t launch_gemv_row(const GemmArgs& g, int num_sms, cudaStream_t s);
 cudaError_t launch_gemv_col(const GemmArgs& g, int num_sms, cudaStream_t s);
 cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s);
+// 32 x 32 tiles with plain loads for products too small to fill the GPU
+// (any layout); grid rows: ceil(M / 32) <= 65535.
+cudaError_t launch_small(const GemmArgs& g, cudaStream_t s);
+constexpr int64_t kSmallMaxRows = 65535 * 32;
 // out (cols x rows, dense, ld = rows) = in (rows x cols, ld) transposed.
 cudaError_t launch_transpose(const float* in, int64_t ld, int64_t rows,
                              int64_t cols, float* out, cudaStream_t s);

@@ -37,6 +37,8 @@ constexpr int64_t kTf32PairMinWork = 256;
 // beats the pairs' stream-K split (1024^3: 29 vs 35 us), with longer k the
 // pairs win (1024 x 1024 x 4096: 59 vs 78 us).
 constexpr int64_t kSplitMaxTiles = 76;
+// Up to this many multiply-adds the small-tile kernel takes the product.
+constexpr int64_t kSmallMaxMacs = int64_t(1) << 23;
 constexpr int64_t kSplitMaxSlices = 32;
 
 int64_t pair_work(int64_t M, int64_t N, int64_t K, int64_t batch) {
@@ -594,6 +596,13 @@ int plan_call(const Call& c) {
   if (c.M == 1) return c.op_b ? SGEMM_PATH_GEMV_COL : SGEMM_PATH_GEMV_ROW;
   if (c.N == 1)
     return gemv_col_as_row(c) ? SGEMM_PATH_GEMV_ROW : SGEMM_PATH_GEMV_COL;
+  // Products too small to fill the GPU: the 32 x 32 tile kernel, in either
+  // math mode (measured faster than every other path up to about 2^23
+  // multiply-adds: 127 x 129 x 33 in 7.7 us against 16.8, 128^3 10.3 against
+  // 15.3; at 256^3 the tensor kernel ties, above it wins).
+  if (double(c.M) * double(c.N) * double(c.K) <= double(kSmallMaxMacs) &&
+      c.M <= kSmallMaxRows)
+    return SGEMM_PATH_SMALL;
   const int64_t tiles = ((c.M + kTileM - 1) / kTileM) *
                         ((c.N + kTileN - 1) / kTileN);
   // Operands the tensor maps cannot take (row stride or base not 16-byte
@@ -787,6 +796,11 @@ int run_call(const Call& call, void* stream, int path) {
       rc = make_row_major(g, lease);
       if (rc != SGEMM_OK) return rc;
       return to_status(launch_naive(g, s));
+    case SGEMM_PATH_SMALL:
+      if (call.M > kSmallMaxRows) return SGEMM_ERR_PATH;
+      rc = make_row_major(g, lease);
+      if (rc != SGEMM_OK) return rc;
+      return to_status(launch_small(g, s));
     default:
       return SGEMM_ERR_PATH;
   }
@@ -939,6 +953,8 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
     }
     case SGEMM_PATH_TILED_LDG:
       return to_status(launch_tiled_ldg(g, st->status, s));
+    case SGEMM_PATH_SMALL:
+      return to_status(launch_small(g, s));
     case SGEMM_PATH_TF32X3:
       return run_tf32x3(g, *st, s, false, nullptr);
     case SGEMM_PATH_TF32X3_PAIR: {
@@ -1270,6 +1286,7 @@ const char* sgemm_path_name(int path) {
     case SGEMM_PATH_GEMV_ROW: return "gemv_row";
     case SGEMM_PATH_GEMV_COL: return "gemv_col";
     case SGEMM_PATH_NAIVE: return "naive";
+    case SGEMM_PATH_SMALL: return "small";
     case SGEMM_PATH_TF32X3: return "tf32x3";
     case SGEMM_PATH_TF32X3_PAIR: return "tf32x3_pair";
     default: return "?";

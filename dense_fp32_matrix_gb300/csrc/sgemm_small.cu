@@ -146,6 +146,77 @@ k_gemv_col(const float* __restrict__ A, long long lda,
   }
 }
 
+// Products too small to fill the GPU: 32 x 32 tiles over 128 threads,
+// each a 2 x 4 patch (rows ty and ty + 16, four adjacent columns); k in
+// chunks of 32 through shared memory, the next chunk held in registers
+// while the current one computes (the register prefetch of "GEMM from
+// naive to tiled", section 六). Plain predicated loads, coalesced along k
+// for A and along n for B, so any alignment and leading dimension; only
+// k < K is summed. A is stored transposed in shared memory with one float
+// of padding per row, so the transposing stores hit distinct banks.
+constexpr int SM_T = 32;
+constexpr int SM_THREADS = 128;
+constexpr int SM_KC = 32;
+
+__global__ void __launch_bounds__(SM_THREADS)
+k_small(const float* __restrict__ A, long long lda,
+        const float* __restrict__ B, long long ldb, float* __restrict__ C,
+        long long ldc, int M, int N, int K, Scale sc) {
+  __shared__ float As[SM_KC][SM_T + 1];             // As[k][row]
+  __shared__ __align__(16) float Bs[SM_KC][SM_T];   // Bs[k][col]
+  const int tid = threadIdx.x;
+  const int m0 = blockIdx.y * SM_T, n0 = blockIdx.x * SM_T;
+  const int lk = tid & 31, lr = tid >> 5;  // loader lane: k (A) / n (B)
+  float ra[SM_KC * SM_T / SM_THREADS], rb[SM_KC * SM_T / SM_THREADS];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int q = 0; q < SM_KC * SM_T / SM_THREADS; ++q) {
+      const int r = m0 + lr + 4 * q, ka = k0 + lk;
+      ra[q] = (r < M && ka < K) ? A[(long long)r * lda + ka] : 0.f;
+      const int kb = k0 + lr + 4 * q, n = n0 + lk;
+      rb[q] = (kb < K && n < N) ? B[(long long)kb * ldb + n] : 0.f;
+    }
+  };
+  const int ty = tid >> 3, tx = tid & 7;   // 16 x 8 threads
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  load(0);
+  for (int k0 = 0; k0 < K; k0 += SM_KC) {
+    __syncthreads();  // the previous chunk has been read
+#pragma unroll
+    for (int q = 0; q < SM_KC * SM_T / SM_THREADS; ++q) {
+      As[lk][lr + 4 * q] = ra[q];
+      Bs[lr + 4 * q][lk] = rb[q];
+    }
+    __syncthreads();
+    if (k0 + SM_KC < K) load(k0 + SM_KC);
+    const int kn = min(SM_KC, K - k0);
+#pragma unroll 8
+    for (int k = 0; k < kn; ++k) {
+      const float a0 = As[k][ty], a1 = As[k][ty + 16];
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[k][4 * tx]);
+      acc[0][0] = fmaf(a0, b.x, acc[0][0]);
+      acc[0][1] = fmaf(a0, b.y, acc[0][1]);
+      acc[0][2] = fmaf(a0, b.z, acc[0][2]);
+      acc[0][3] = fmaf(a0, b.w, acc[0][3]);
+      acc[1][0] = fmaf(a1, b.x, acc[1][0]);
+      acc[1][1] = fmaf(a1, b.y, acc[1][1]);
+      acc[1][2] = fmaf(a1, b.z, acc[1][2]);
+      acc[1][3] = fmaf(a1, b.w, acc[1][3]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = m0 + ty + 16 * i;
+    if (r >= M) continue;
+    float* crow = C + (long long)r * ldc;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = n0 + 4 * tx + e;
+      if (c < N) crow[c] = epi1(acc[i][e], crow + c, sc);
+    }
+  }
+}
+
 __global__ void k_naive(const float* __restrict__ A, long long lda,
                         const float* __restrict__ B, long long ldb,
                         float* __restrict__ C, long long ldc, int M, int N,
@@ -194,16 +265,26 @@ k_transpose(const float* __restrict__ in, long long ld, int rows, int cols,
 // dst (rows x cols, ld dld) = src (rows x cols, ld sld): a repack with
 // another leading dimension. Row-wise grid-stride copy, coalesced on both
 // sides; the padding of dst is not written.
-__global__ void k_repack(const float* __restrict__ src, long long sld,
-                         int rows, int cols, float* __restrict__ dst,
-                         long long dld) {
-  for (long long r = blockIdx.y; r < rows; r += gridDim.y)
-    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols;
-         c += gridDim.x * blockDim.x)
-      dst[r * dld + c] = src[r * sld + c];
+// dst = src with another row stride: a block copies 8 rows, each thread
+// one column of them per pass, its 8 loads issued before its stores so
+// that they are in flight together (the plain one-element copy left the
+// loads waiting one by one on memory).
+constexpr int RP_ROWS = 8;
+__global__ void __launch_bounds__(256)
+k_repack(const float* __restrict__ src, long long sld, int rows, int cols,
+         float* __restrict__ dst, long long dld) {
+  const long long r0 = (long long)blockIdx.x * RP_ROWS;
+  for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+    float v[RP_ROWS];
+#pragma unroll
+    for (int i = 0; i < RP_ROWS; ++i)
+      v[i] = r0 + i < rows ? __ldcs(src + (r0 + i) * sld + c) : 0.f;
+#pragma unroll
+    for (int i = 0; i < RP_ROWS; ++i)
+      if (r0 + i < rows) dst[(r0 + i) * dld + c] = v[i];
+  }
 }
 
-// C = beta * C (beta == 0: C = 0 without reading it).
 __global__ void k_scale_c(float* __restrict__ C, long long ldc, int M, int N,
                           float beta) {
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
@@ -264,6 +345,15 @@ cudaError_t launch_gemv_col(const GemmArgs& g, int num_sms, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_small(const GemmArgs& g, cudaStream_t s) {
+  const dim3 grid(unsigned((g.N + SM_T - 1) / SM_T),
+                  unsigned((g.M + SM_T - 1) / SM_T));
+  k_small<<<grid, SM_THREADS, 0, s>>>(g.A, (long long)g.lda, g.B,
+                                       (long long)g.ldb, g.C, (long long)g.ldc,
+                                       int(g.M), int(g.N), int(g.K), g.sc);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s) {
   const dim3 block(32, 8);
   long long gy = (g.M + 7) / 8;
@@ -289,11 +379,9 @@ cudaError_t launch_repack(const float* src, int64_t sld, int64_t rows,
                           int64_t cols, float* dst, int64_t dld,
                           cudaStream_t s) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  const int64_t gx = (cols + 255) / 256;
-  const dim3 grid(unsigned(gx < 64 ? gx : 64),
-                  unsigned(rows < 65535 ? rows : 65535));
-  k_repack<<<grid, 256, 0, s>>>(src, (long long)sld, int(rows), int(cols), dst,
-                                (long long)dld);
+  const int64_t blocks = (rows + RP_ROWS - 1) / RP_ROWS;  // < 2^31 rows / 8
+  k_repack<<<unsigned(blocks), 256, 0, s>>>(src, (long long)sld, int(rows),
+                                            int(cols), dst, (long long)dld);
   return cudaGetLastError();
 }
 

@@ -114,7 +114,9 @@ extern "C" {
 #define SGEMM_PATH_NAIVE 5      /* one thread per output (debug baseline)  */
 #define SGEMM_PATH_TF32X3 6     /* tensor cores, 3 TF32 products (aligned)  */
 #define SGEMM_PATH_TF32X3_PAIR 7 /* same on 2-SM pairs, 256 x 256 tiles     */
-#define SGEMM_PATH_COUNT 8
+#define SGEMM_PATH_SMALL 8      /* 32 x 32 tiles, plain loads: products too
+                                   small to fill the GPU (any layout)      */
+#define SGEMM_PATH_COUNT 9
 
 /*
  * sgemm: C = A * B as described above, on `stream`.

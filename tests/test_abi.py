@@ -74,7 +74,11 @@ C16 = 0x7f0020000000
     (512, 512, 4096, 4096, 512, 512, A16, B16, "tf32x3_pair"),  # long K: split
     # ld % 4 != 0: repacked for the tensor path (large enough)
     (4095, 4097, 1023, 1023, 4097, 4097, A16, B16, "tf32x3_pair"),
-    (127, 129, 33, 33, 129, 129, A16, B16, "tiled_ldg"),  # too small to repack
+    # at most 2^23 multiply-adds: the small-tile kernel, any layout
+    (127, 129, 33, 33, 129, 129, A16, B16, "small"),
+    (128, 128, 128, 128, 128, 128, A16, B16, "small"),
+    (300, 200, 20, 20, 200, 200, A16, B16, "small"),
+    (255, 257, 129, 129, 257, 257, A16, B16, "tiled_ldg"),  # too small to repack
     (4096, 4096, 4096, 4096, 4096, 4096, A16 + 4, B16, "tf32x3_pair"),  # align
     (4096, 4096, 4096, 4100, 4096, 4096, A16, B16, "tf32x3_pair"),  # pitch
     (1, 4096, 4096, 4096, 4096, 4096, A16, B16, "gemv_row"),
@@ -145,7 +149,9 @@ def test_sgemm_rejects_bad_arguments_before_touching_a_device(lib):
     # lda % 4 != 0: A repacked (as stored) for the tensor path
     ("T", "N", 4096, 4096, 4096, 4097, 4096, A16, B16, "tf32x3_pair"),
     # A misaligned and too small to repack: the cp.async tile kernel
-    ("N", "T", 100, 20, 64, 64, 64, A16 + 4, B16, "tiled_ldg"),
+    ("N", "T", 400, 300, 72, 72, 72, A16 + 4, B16, "tiled_ldg"),
+    # at most 2^23 multiply-adds: the small-tile kernel
+    ("N", "T", 100, 20, 64, 64, 64, A16 + 4, B16, "small"),
     ("N", "T", 1, 4096, 4096, 4096, 4096, A16, B16, "gemv_col"),  # a * B^T
     ("T", "N", 1, 4096, 4096, 1, 4096, A16, B16, "gemv_row"),
     # c = A^T b with dense c and b: the row kernel on A as stored

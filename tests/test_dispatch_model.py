@@ -7,6 +7,8 @@ The rules, in order:
     transposed (c = a Bᵀ are B's rows times a);
   * N == 1: the column kernel, or the row kernel for c = Aᵀ b with A stored
     transposed and c, b contiguous (cᵀ = bᵀ A);
+  * at most 2^23 multiply-adds (and M within the kernel's grid): the
+    small-tile kernel, in either math mode;
   * in the default math mode, operands that TMA can map (16-byte base and
     row stride) or products of at least 2^24 multiply-adds (repacked first)
     take the tensor cores: 2-SM pairs from 256 units of work (256×256 tiles
@@ -35,6 +37,8 @@ def model(op_a, op_b, M, N, K, lda, ldb, ldc, a, b, math):
     if N == 1:
         return "gemv_row" if (ta and ldc == 1 and (tb or ldb == 1)) \
             else "gemv_col"
+    if M * N * K <= (1 << 23) and M <= 65535 * 32:
+        return "small"
     aligned = tma_ok(a, lda) and tma_ok(b, ldb)
     if (aligned or M * N * K >= (1 << 24)) and math == "auto":
         work = -(-M // 256) * -(-N // 256) * -(-K // 32)

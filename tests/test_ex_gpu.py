@@ -71,7 +71,8 @@ def run_ex(op_a, op_b, M, N, K, alpha, beta, kind="uniform", seed=0,
     return compare(kind, got[rows], ref, S, what + " rows")
 
 
-PATHS_2D = ["auto", "tf32x3", "tf32x3_pair", "tiled_tma", "tiled_ldg", "naive"]
+PATHS_2D = ["auto", "tf32x3", "tf32x3_pair", "tiled_tma", "tiled_ldg", "naive",
+            "small"]
 
 
 @pytest.mark.parametrize("path", PATHS_2D)

@@ -38,7 +38,7 @@ MULTI_TILE = [(300, 200, 20), (257, 383, 129), (128, 128, 32), (129, 257, 33),
               (640, 384, 96), (1000, 1000, 1000), (384, 256, 24)]
 
 
-@pytest.mark.parametrize("path", ["auto", "tiled_ldg", "naive"])
+@pytest.mark.parametrize("path", ["auto", "tiled_ldg", "naive", "small"])
 @pytest.mark.parametrize("mnk", MULTI_TILE, ids=str)
 @pytest.mark.parametrize("kind", ["uniform", "integers"])
 def test_multi_tile_paths(path, mnk, kind):
@@ -56,7 +56,7 @@ def test_tma_path_forced(mnk):
 SIZES = (1, 2, 3, 4, 5, 7, 8, 9, 16, 17, 31, 33)
 
 
-@pytest.mark.parametrize("path", ["auto", "tiled_ldg", "naive"])
+@pytest.mark.parametrize("path", ["auto", "tiled_ldg", "naive", "small"])
 def test_brute_force_tiny_shapes(path):
     for M, N, K in itertools.product(SIZES, SIZES, SIZES):
         run_case(M, N, K, kind="integers", seed=M * 10000 + N * 100 + K,
@@ -189,3 +189,16 @@ def test_watchdog_timeout_is_reported_and_context_survives():
     assert rc == dfm.STATUS["SGEMM_ERR_WATCHDOG"]
     assert dfm.sgemm_watchdog_status()[0] == 0   # read-and-clear
     run_case(130, 130, 40, "integers", 3)          # device still usable
+
+
+# The 32 x 32 small-tile kernel on padded, misaligned and multi-chunk k
+# layouts (sentinels around C, NaN in the pitch padding of A and B).
+@pytest.mark.parametrize("mnk", [(127, 129, 33), (64, 64, 64), (33, 65, 97),
+                                 (256, 256, 256), (1, 40, 7), (40, 1, 7)],
+                         ids=str)
+def test_small_path_layouts(mnk):
+    M, N, K = mnk
+    for kind in ("uniform", "integers"):
+        run_case(M, N, K, kind=kind, seed=M + N + K, path="small")
+    run_case(M, N, K, kind="uniform", seed=3, path="small", lda=K + 3,
+             ldb=N + 5, ldc=N + 1, offsets=(1, 2, 3))
