@@ -73,6 +73,10 @@ KERNEL_SOURCES = {
                       "kernels.h"],
     "k_gemv_row_tma": ["sgemm_gemv.cu", "ptx.cuh", "kernels.h"],
     "k_gemv_col_tma": ["sgemm_gemv.cu", "ptx.cuh", "kernels.h"],
+    "k_tiled_ldg": ["sgemm_tiled.cu", "ptx.cuh", "kernels.h"],
+    "k_small": ["sgemm_small.cu", "ptx.cuh", "kernels.h"],
+    "k_gemv_row": ["sgemm_small.cu", "ptx.cuh", "kernels.h"],
+    "k_gemv_col": ["sgemm_small.cu", "ptx.cuh", "kernels.h"],
 }
 
 
@@ -438,6 +442,7 @@ def run_gpu(args, w):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    launches0 = dfm.sgemm_launch_count()
     with ClockSampler(dev) as clocks:
         clocks.start()
         for i in range(args.steps):
@@ -447,6 +452,7 @@ def run_gpu(args, w):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         clocks.stop()
+    launches = dfm.sgemm_launch_count() - launches0
     if world > 1:
         torch.distributed.barrier()
     st, site = dfm.sgemm_watchdog_status()
@@ -508,6 +514,14 @@ def run_gpu(args, w):
               "tf32x3": "k_tf32x3", "tf32x3_pair": "k_tf32x3_pair",
               "gemv_row": "k_gemv_row_tma", "gemv_col": "k_gemv_col_tma",
               "small": "k_small", "naive": "k_naive"}.get(plan, plan)
+    # The vector paths take their TMA kernels only for 16-byte aligned
+    # operands (the same test as the library's); else the plain ones.
+    if plan == "gemv_row" and not (pB % 16 == 0 and ldb % 4 == 0
+                                   and pA % 16 == 0):
+        kernel = "k_gemv_row"
+    if plan == "gemv_col" and not (pA % 16 == 0 and lda % 4 == 0
+                                   and ldb == 1 and pB % 16 == 0):
+        kernel = "k_gemv_col"
     if plan.startswith("tf32x3"):
         # Roofline of the tensor kernels: the dense TF32 rate of the tensor
         # cores at the SM clock of the timed region (ncu's per-clock rate of
@@ -544,13 +558,30 @@ def run_gpu(args, w):
         # a stream over the matrix: bound by HBM bandwidth
         hbm, src = measured_hbm_gbs()
         gbs = 4 * (M * K + K * N + M * N) / (ms_step * 1e-3) / 1e9
+        # Context: PyTorch's own reduction over the same matrix, timed the
+        # same way (flush, events): another kernel that streams these bytes
+        # once from a cold L2, launch and ramp included.
+        X = A if M > 1 else B
+        sink = torch.empty((), device="cuda")
+        rms = time_steps(lambda: torch.sum(X, dim=(0, 1), out=sink), flush,
+                         stream, max(5, min(args.steps, 100)), 3)
+        r_ms = statistics.median(rms)
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                 "frac": gbs / hbm,
                 "traffic": recorded_traffic(kernel, w["name"]),
                 "kernel": kernel,
                 "peak_basis": "HBM copy bandwidth %.1f GB/s (%s, "
                               "MEASURED_PEAKS.json); algorithmic bytes "
-                              "4(MK + KN + MN)" % (hbm, src)}
+                              "4(MK + KN + MN)" % (hbm, src),
+                "context_torch_sum": {
+                    "kernel": "torch.sum over the same %d x %d matrix"
+                              % tuple(X.shape),
+                    "ms_median": r_ms,
+                    "gbs": 4 * X.numel() / (r_ms * 1e-3) / 1e9,
+                    "gemv_ms_median": statistics.median(ms),
+                    "basis": "same flush and event timing as the product; "
+                             "a library reduction over the same bytes, "
+                             "for comparison"}}
     else:
         roof = {"bound": "alu", "achieved": tflops,
                 "peak": ffma_peak_at(clock_mhz), "unit": "TFLOP/s",
@@ -634,7 +665,11 @@ def run_gpu(args, w):
                 "api": "sgemm_host (pinned host buffers, 2-D async copies "
                        "on the stream)",
                 "path": e2e_plan},
-        "gpu_launches": args.steps,
+        "gpu_launches": launches,
+        "gpu_launches_basis": {"per_step": launches / args.steps,
+                               "how": "the library's own count of the kernel "
+                                      "launches it issued (sgemm_launch_count) "
+                                      "across the timed region"},
         "ms_min": min(ms), "ms_median": statistics.median(ms),
     }
     if plan in ("tiled_tma", "tiled_ldg"):

@@ -16,7 +16,7 @@ __all__ = [
     "sgemm_ex", "sgemm_plan_ex", "sgemm_strided_batched", "OPS",
     "sgemm_noalloc", "sgemm_set_math_mode", "MATH",
     "sgemm_watchdog_status", "sgemm_watchdog_selftest",
-    "sgemm_workspace_info", "sgemm_status_string", "sgemm_path_name", "sgemm_version", "matmul",
+    "sgemm_workspace_info", "sgemm_status_string", "sgemm_path_name", "sgemm_version", "sgemm_launch_count", "matmul",
     "PATHS", "STATUS",
 ]
 
@@ -198,6 +198,11 @@ def sgemm_path_name(path: int) -> str:
 
 def sgemm_version() -> int:
     return int(_native.lib().sgemm_version())
+
+
+def sgemm_launch_count() -> int:
+    """Kernel launches the library has issued in this process."""
+    return int(_native.lib().sgemm_launch_count())
 
 
 def matmul(A, B, out=None, path="auto", stream=None):

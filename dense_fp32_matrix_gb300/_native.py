@@ -56,6 +56,7 @@ _SIGNATURES = {
     "sgemm_status_string": ([_int], ctypes.c_char_p),
     "sgemm_path_name": ([_int], ctypes.c_char_p),
     "sgemm_version": ([], _int),
+    "sgemm_launch_count": ([], ctypes.c_uint64),
 }
 
 

@@ -8,6 +8,15 @@
 
 namespace dfm {
 
+// Kernel launches this library has issued in this process (all devices and
+// streams). Every launcher passes the result of its launch through
+// counted(), which adds one when the launch was accepted.
+void count_launch();
+inline cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
 // The BLAS epilogue of every kernel: C = alpha * acc + beta * C_old, with
 // C_old not read when beta == 0 (alpha = 1, beta = 0 stores acc exactly).
 struct Scale {

@@ -16,6 +16,9 @@
 #include "ptx.cuh"
 
 namespace dfm {
+
+std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 namespace {
 
 // Per-device status word of the bounded waits (see ptx.cuh).
@@ -26,6 +29,10 @@ std::atomic<int> g_math_mode{SGEMM_MATH_AUTO};
 // Misaligned operands: repacked for the tensor path from this many
 // multiply-adds on (below, the CUDA-core kernel that reads them as they are).
 constexpr int64_t kTf32RepackMinMacs = int64_t(1) << 24;
+// The same for the CUDA-core path: from this size the TMA-fed tile kernel
+// (about 80% of the FMA peak) on repacked copies beats the any-layout
+// kernel (about 57% on 4095 x 4097 x 1023) by more than the copies cost.
+constexpr int64_t kFfmaRepackMinMacs = int64_t(1) << 32;
 // From this much work on (256 x 256 tiles x k-slices of 32) the 2-SM pair
 // kernel, which splits k-slices over all clusters when tiles are few, beats
 // one 1-SM block per 128 x 128 tile (measured: every long-K shape of few
@@ -620,10 +627,16 @@ int plan_call(const Call& c) {
   // first copied row-major (dense, ld = its width) into the workspace.
   const bool a_ok = c.op_a ? c.K % 4 == 0 : tma_operand_ok(a, c.lda);
   const bool b_ok = c.op_b ? c.N % 4 == 0 : tma_operand_ok(b, c.ldb);
+  // Untransposed operands TMA cannot map are repacked to 16-byte rows
+  // first when the product is large enough to pay for it.
+  const bool repack = !c.op_a && !c.op_b &&
+                      double(c.M) * double(c.N) * double(c.K) >=
+                          double(kFfmaRepackMinMacs);
   // The stream-K schedule counts k-slice iterations in 32 bits.
   const int64_t iters = tiles * ((c.K + kTileK - 1) / kTileK);
-  return a_ok && b_ok && iters < (1ll << 31) ? SGEMM_PATH_TILED_TMA
-                                             : SGEMM_PATH_TILED_LDG;
+  return ((a_ok && b_ok) || repack) && iters < (1ll << 31)
+             ? SGEMM_PATH_TILED_TMA
+             : SGEMM_PATH_TILED_LDG;
 }
 
 int plan_path(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -717,7 +730,8 @@ int run_call(const Call& call, void* stream, int path) {
         launch_scale_c(call.C, call.ldc, call.M, call.N, call.beta, s));
   }
 
-  if (path == SGEMM_PATH_AUTO) path = plan_call(call);
+  const bool chosen = path == SGEMM_PATH_AUTO;
+  if (chosen) path = plan_call(call);
   GemmArgs g{call.M,   call.N, call.K,   call.A, call.lda,
              call.B,   call.ldb, call.C, call.ldc};
   g.sc.alpha = call.alpha;
@@ -773,8 +787,15 @@ int run_call(const Call& call, void* stream, int path) {
       rc = make_row_major(g, lease);
       if (rc != SGEMM_OK) return rc;
       if (!tma_operand_ok(reinterpret_cast<uint64_t>(g.A), g.lda) ||
-          !tma_operand_ok(reinterpret_cast<uint64_t>(g.B), g.ldb))
-        return SGEMM_ERR_PATH;
+          !tma_operand_ok(reinterpret_cast<uint64_t>(g.B), g.ldb)) {
+        // Only the library's own choice repacks (plan_call picks this path
+        // for misaligned operands only when neither is transposed, so the
+        // workspace copy below is the only one); a forced path on layouts
+        // TMA cannot map is refused.
+        if (!chosen || call.op_a || call.op_b) return SGEMM_ERR_PATH;
+        rc = make_tensor_ready(g, lease);
+        if (rc != SGEMM_OK) return rc;
+      }
       if (plan_stream_k(g.M, g.N, g.K, 1).total_iters >= (1ll << 31))
         return SGEMM_ERR_TOO_LARGE;
       CUtensorMap tmA, tmB;
@@ -924,10 +945,11 @@ int run_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
     return to_status(cudaMemset2DAsync(C, size_t(ldc) * 4, 0, size_t(N) * 4,
                                        size_t(M), s));
   int path = plan_path(M, N, K, lda, ldb, a, b);
-  // The tensor paths take misaligned operands through a repacked copy,
-  // which needs device memory: here such operands go to the any-layout
-  // tile kernel instead.
-  if ((path == SGEMM_PATH_TF32X3 || path == SGEMM_PATH_TF32X3_PAIR) &&
+  // The tensor paths and the TMA tile kernel take misaligned operands
+  // through a repacked copy, which needs device memory: here such operands
+  // go to the any-layout tile kernel instead.
+  if ((path == SGEMM_PATH_TF32X3 || path == SGEMM_PATH_TF32X3_PAIR ||
+       path == SGEMM_PATH_TILED_TMA) &&
       !(tma_operand_ok(a, lda) && tma_operand_ok(b, ldb)))
     path = SGEMM_PATH_TILED_LDG;
   const GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc};
@@ -1294,5 +1316,9 @@ const char* sgemm_path_name(int path) {
 }
 
 int sgemm_version(void) { return 100; }
+
+uint64_t sgemm_launch_count(void) {
+  return dfm::g_launches.load(std::memory_order_relaxed);
+}
 
 }  // extern "C"

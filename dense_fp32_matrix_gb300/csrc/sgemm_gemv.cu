@@ -38,6 +38,9 @@ constexpr int GR_A_STAGE = GR_ROWS * 4;           // 256 B of a
 constexpr int GR_MAX_CLUSTER = 8;
 constexpr size_t GR_SMEM =
     size_t(kStages) * (GR_STAGE + GR_A_STAGE) + 64 + 128;
+// Tiled TMA writes shared memory at 128-byte aligned addresses only.
+static_assert(GR_STAGE % 128 == 0 && GR_A_STAGE % 128 == 0,
+              "row-kernel stage slots must keep 128-byte alignment");
 
 __global__ void __launch_bounds__(kThreads)
 k_gemv_row_tma(const __grid_constant__ CUtensorMap tmB,
@@ -145,6 +148,8 @@ constexpr int GC_A_STAGE = GC_ROWS * GC_K * 4;    // 16 KiB
 constexpr int GC_B_STAGE = GC_K * 4;              // 1 KiB
 constexpr size_t GC_SMEM =
     size_t(kStages) * (GC_A_STAGE + GC_B_STAGE) + 64 + 128;
+static_assert(GC_A_STAGE % 128 == 0 && GC_B_STAGE % 128 == 0,
+              "col-kernel stage slots must keep 128-byte alignment");
 static_assert(GC_K / 4 == 4 * GC_LANES, "4 float4 per lane per stage");
 
 __global__ void __launch_bounds__(kThreads)
@@ -259,9 +264,9 @@ cudaError_t launch_gemv_row_tma(const GemmArgs& g, const CUtensorMap& tmB,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_gemv_row_tma, tmB, tma_, g.C, int(g.N),
+  return counted(cudaLaunchKernelEx(&cfg, k_gemv_row_tma, tmB, tma_, g.C, int(g.N),
                             int(g.K), int(pl.k_per_block), pl.cluster, g.sc,
-                            status);
+                            status));
 }
 
 cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
@@ -270,7 +275,7 @@ cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
   const unsigned blocks = unsigned((g.M + GC_ROWS - 1) / GC_ROWS);
   k_gemv_col_tma<<<blocks, kThreads, GC_SMEM, s>>>(
       tmA, tmb, g.C, (long long)g.ldc, int(g.M), int(g.K), g.sc, status);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace dfm

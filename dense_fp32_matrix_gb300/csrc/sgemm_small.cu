@@ -70,9 +70,27 @@ k_gemv_row(const float* __restrict__ a, const float* __restrict__ B,
     }
   } else {
     // Any layout: the 4 lanes of a group read 16 consecutive columns, lane
-    // q columns n0 + q + 4 e, one float each, predicated on N.
+    // q columns n0 + q + 4 e, one float each, predicated on N. ROW_UNROLL
+    // rows are loaded before any is used, so that their loads are in
+    // flight together; each column still sums its rows in k order.
     const int n0 = blockIdx.x * ROW_COLS;
-    for (int k = grp; k < K; k += ROW_GROUPS) {
+    int k = grp;
+    for (; k + (ROW_UNROLL - 1) * ROW_GROUPS < K; k += ROW_UNROLL * ROW_GROUPS) {
+      float s[ROW_UNROLL], v[ROW_UNROLL][4];
+#pragma unroll
+      for (int u = 0; u < ROW_UNROLL; ++u) {
+        s[u] = __ldg(a + k + u * ROW_GROUPS);
+        const float* row = B + (long long)(k + u * ROW_GROUPS) * ldb + n0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          v[u][e] = n0 + q + 4 * e < N ? __ldg(row + q + 4 * e) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < ROW_UNROLL; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = fmaf(s[u], v[u][e], acc[e]);
+    }
+    for (; k < K; k += ROW_GROUPS) {
       const float s = __ldg(a + k);
       const float* row = B + (long long)k * ldb + n0;
 #pragma unroll
@@ -94,6 +112,7 @@ k_gemv_row(const float* __restrict__ a, const float* __restrict__ B,
 }
 
 constexpr int COL_WARPS = 8;
+constexpr int COL_UNROLL = 8;
 
 template <bool VEC>
 __global__ void __launch_bounds__(COL_WARPS * 32)
@@ -136,7 +155,20 @@ k_gemv_col(const float* __restrict__ A, long long lda,
       for (int kk = 4 * K4 + lane; kk < K; kk += 32)
         acc = fmaf(__ldg(row + kk), __ldg(b + kk), acc);
     } else {
-      for (int k = lane; k < K; k += 32)
+      // Any layout: COL_UNROLL k per lane loaded before use (in flight
+      // together), summed in k order.
+      int k = lane;
+      for (; k + 32 * (COL_UNROLL - 1) < K; k += 32 * COL_UNROLL) {
+        float x[COL_UNROLL], y[COL_UNROLL];
+#pragma unroll
+        for (int u = 0; u < COL_UNROLL; ++u) {
+          x[u] = __ldg(row + k + 32 * u);
+          y[u] = __ldg(b + (long long)(k + 32 * u) * ldb);
+        }
+#pragma unroll
+        for (int u = 0; u < COL_UNROLL; ++u) acc = fmaf(x[u], y[u], acc);
+      }
+      for (; k < K; k += 32)
         acc = fmaf(__ldg(row + k), __ldg(b + (long long)k * ldb), acc);
     }
 #pragma unroll
@@ -263,25 +295,29 @@ k_transpose(const float* __restrict__ in, long long ld, int rows, int cols,
 }
 
 // dst (rows x cols, ld dld) = src (rows x cols, ld sld): a repack with
-// another leading dimension. Row-wise grid-stride copy, coalesced on both
-// sides; the padding of dst is not written.
-// dst = src with another row stride: a block copies 8 rows, each thread
-// one column of them per pass, its 8 loads issued before its stores so
-// that they are in flight together (the plain one-element copy left the
-// loads waiting one by one on memory).
+// another leading dimension, coalesced on both sides; the padding of dst is
+// not written. A block owns 256 columns (one per thread) of a run of 8-row
+// groups; each thread issues its 8 loads before its stores so that they are
+// in flight together. The grid spans columns as well as rows, so a matrix
+// with few rows still fills every SM.
 constexpr int RP_ROWS = 8;
-__global__ void __launch_bounds__(256)
+constexpr int RP_COLS = 256;  // threads per block, one column each
+__global__ void __launch_bounds__(RP_COLS)
 k_repack(const float* __restrict__ src, long long sld, int rows, int cols,
          float* __restrict__ dst, long long dld) {
-  const long long r0 = (long long)blockIdx.x * RP_ROWS;
-  for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+  const int c = blockIdx.x * RP_COLS + threadIdx.x;
+  if (c >= cols) return;  // no block barrier below
+  for (long long r0 = (long long)blockIdx.y * RP_ROWS; r0 < rows;
+       r0 += (long long)gridDim.y * RP_ROWS) {
+    const int n = rows - r0 < RP_ROWS ? int(rows - r0) : RP_ROWS;
     float v[RP_ROWS];
+    const float* p = src + r0 * sld + c;  // row pointers by addition
 #pragma unroll
-    for (int i = 0; i < RP_ROWS; ++i)
-      v[i] = r0 + i < rows ? __ldcs(src + (r0 + i) * sld + c) : 0.f;
+    for (int i = 0; i < RP_ROWS; ++i, p += sld) v[i] = i < n ? __ldcs(p) : 0.f;
+    float* q = dst + r0 * dld + c;
 #pragma unroll
-    for (int i = 0; i < RP_ROWS; ++i)
-      if (r0 + i < rows) dst[(r0 + i) * dld + c] = v[i];
+    for (int i = 0; i < RP_ROWS; ++i, q += dld)
+      if (i < n) *q = v[i];
   }
 }
 
@@ -326,7 +362,7 @@ cudaError_t launch_gemv_row(const GemmArgs& g, int num_sms, cudaStream_t s) {
   else
     k_gemv_row<false><<<blocks, ROW_THREADS, 0, s>>>(g.A, g.B, g.ldb, g.C,
                                                       int(g.N), int(g.K), g.sc);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_gemv_col(const GemmArgs& g, int num_sms, cudaStream_t s) {
@@ -342,7 +378,7 @@ cudaError_t launch_gemv_col(const GemmArgs& g, int num_sms, cudaStream_t s) {
   else
     k_gemv_col<false><<<unsigned(blocks), COL_WARPS * 32, 0, s>>>(
         g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M), int(g.K), g.sc);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_small(const GemmArgs& g, cudaStream_t s) {
@@ -351,7 +387,7 @@ cudaError_t launch_small(const GemmArgs& g, cudaStream_t s) {
   k_small<<<grid, SM_THREADS, 0, s>>>(g.A, (long long)g.lda, g.B,
                                        (long long)g.ldb, g.C, (long long)g.ldc,
                                        int(g.M), int(g.N), int(g.K), g.sc);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s) {
@@ -361,7 +397,7 @@ cudaError_t launch_naive(const GemmArgs& g, cudaStream_t s) {
   const dim3 grid(unsigned((g.N + 31) / 32), unsigned(gy));
   k_naive<<<grid, block, 0, s>>>(g.A, g.lda, g.B, g.ldb, g.C, g.ldc, int(g.M),
                                  int(g.N), int(g.K), g.sc);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_transpose(const float* in, int64_t ld, int64_t rows,
@@ -372,17 +408,19 @@ cudaError_t launch_transpose(const float* in, int64_t ld, int64_t rows,
                   unsigned(row_tiles < 65535 ? row_tiles : 65535));
   k_transpose<<<grid, dim3(TR_TILE, TR_ROWS), 0, s>>>(in, (long long)ld,
                                                       int(rows), int(cols), out);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_repack(const float* src, int64_t sld, int64_t rows,
                           int64_t cols, float* dst, int64_t dld,
                           cudaStream_t s) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  const int64_t blocks = (rows + RP_ROWS - 1) / RP_ROWS;  // < 2^31 rows / 8
-  k_repack<<<unsigned(blocks), 256, 0, s>>>(src, (long long)sld, int(rows),
-                                            int(cols), dst, (long long)dld);
-  return cudaGetLastError();
+  const int64_t groups = (rows + RP_ROWS - 1) / RP_ROWS;
+  const dim3 grid(unsigned((cols + RP_COLS - 1) / RP_COLS),
+                  unsigned(groups < 65535 ? groups : 65535));
+  k_repack<<<grid, RP_COLS, 0, s>>>(src, (long long)sld, int(rows), int(cols),
+                                    dst, (long long)dld);
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_scale_c(float* C, int64_t ldc, int64_t M, int64_t N,
@@ -391,13 +429,13 @@ cudaError_t launch_scale_c(float* C, int64_t ldc, int64_t M, int64_t N,
   long long gy = M < 65535 ? M : 65535;
   k_scale_c<<<dim3(unsigned((N + 255) / 256), unsigned(gy)), 256, 0, s>>>(
       C, (long long)ldc, int(M), int(N), beta);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_watchdog_selftest(int* status, uint64_t limit_ns,
                                      cudaStream_t s) {
   k_watchdog_selftest<<<1, 32, 0, s>>>(status, limit_ns);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace dfm

@@ -1530,22 +1530,22 @@ cudaError_t launch_tf32x3_pair(const GemmArgs& g, const CUtensorMap& tmA,
   cfg.numAttrs = 1;
   const bool early = pl.dp_tiles > 0 && pl.sk_tiles > 0;
   switch (g.op_a * 4 + g.op_b * 2 + (early ? 1 : 0)) {
-    case 0: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0, false>, tmA,
-                                      tmB, mapC, p);
-    case 1: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0, true>, tmA,
-                                      tmB, mapC, p);
-    case 2: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1, false>, tmA,
-                                      tmB, mapC, p);
-    case 3: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1, true>, tmA,
-                                      tmB, mapC, p);
-    case 4: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0, false>, tmA,
-                                      tmB, mapC, p);
-    case 5: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0, true>, tmA,
-                                      tmB, mapC, p);
-    case 6: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1, false>, tmA,
-                                      tmB, mapC, p);
-    default: return cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1, true>, tmA,
-                                       tmB, mapC, p);
+    case 0: return counted(cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0, false>, tmA,
+                                       tmB, mapC, p));
+    case 1: return counted(cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 0, true>, tmA,
+                                       tmB, mapC, p));
+    case 2: return counted(cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1, false>, tmA,
+                                       tmB, mapC, p));
+    case 3: return counted(cudaLaunchKernelEx(&cfg, k_tf32x3_pair<0, 1, true>, tmA,
+                                       tmB, mapC, p));
+    case 4: return counted(cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0, false>, tmA,
+                                       tmB, mapC, p));
+    case 5: return counted(cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 0, true>, tmA,
+                                       tmB, mapC, p));
+    case 6: return counted(cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1, false>, tmA,
+                                       tmB, mapC, p));
+    default: return counted(cudaLaunchKernelEx(&cfg, k_tf32x3_pair<1, 1, true>, tmA,
+                                        tmB, mapC, p));
   }
 }
 
@@ -1596,12 +1596,12 @@ cudaError_t launch_tf32x3(const GemmArgs& g, const CUtensorMap& tmA,
     case 2: go(k_tf32x3<1, 0>); break;
     default: go(k_tf32x3<1, 1>); break;
   }
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = counted(cudaGetLastError());
   if (e != cudaSuccess || splits == 1) return e;
   k_splitk_reduce<<<dim3(grid, XM * XN / 4 / 256), 256, 0, s>>>(
       part4, splits, g.C, int(g.M), int(g.N), (long long)g.ldc, tiles_m,
       tiles_n, vec ? 1 : 0, g.sc, (long long)g.stride_c);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace dfm

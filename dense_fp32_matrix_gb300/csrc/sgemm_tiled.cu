@@ -684,7 +684,7 @@ cudaError_t launch_tiled_tma(const GemmArgs& g, const CUtensorMap& tmA,
   p.sc = g.sc;
   p.status = status;
   k_tiled_tma<<<pl.grid, T_THREADS, TMA_SMEM_BYTES, s>>>(tmA, tmB, g.C, p);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_tiled_ldg(const GemmArgs& g, int* status, cudaStream_t s) {
@@ -694,7 +694,7 @@ cudaError_t launch_tiled_ldg(const GemmArgs& g, int* status, cudaStream_t s) {
   k_tiled_ldg<<<grid, LdgCfg::NT, LDG_SMEM_BYTES, s>>>(
       g.A, (long long)g.lda, g.B, (long long)g.ldb, g.C, int(g.M), int(g.N),
       int(g.K), (long long)g.ldc, vec_ok(g) ? 1 : 0, g.sc);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace dfm

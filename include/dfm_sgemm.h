@@ -331,6 +331,16 @@ int sgemm_watchdog_selftest(void* stream, int64_t timeout_ns);
  */
 int sgemm_workspace_info(int* count, int64_t* bytes);
 
+/*
+ * sgemm_launch_count: how many kernel launches this library has issued in
+ * this process, on all devices and streams, counting each launch the CUDA
+ * runtime accepted (memsets and copies are not kernels and are not
+ * counted). Host only, never fails; the difference of two readings is the
+ * number of the library's kernels enqueued between them. No counterpart on
+ * the pages (a diagnostic of this library's work).
+ */
+uint64_t sgemm_launch_count(void);
+
 /* Human-readable name of a status code (static storage). */
 const char* sgemm_status_string(int status);
 

@@ -32,7 +32,8 @@ def test_header_declares_the_entry_points():
               "sgemm_strided_batched", "sgemm_strided_batched_path",
               "sgemm_set_math_mode",
               "sgemm_watchdog_status", "sgemm_watchdog_selftest",
-              "sgemm_status_string", "sgemm_path_name", "sgemm_version"):
+              "sgemm_status_string", "sgemm_path_name", "sgemm_version",
+              "sgemm_launch_count", "sgemm_workspace_info"):
         assert n in names
 
 
@@ -51,6 +52,8 @@ def test_exports_are_plain_c(lib):
 
 def test_version_and_strings(lib):
     assert dfm.sgemm_version() >= 100
+    # host-only counter: no GPU needed, nothing launched in a CPU session
+    assert dfm.sgemm_launch_count() >= 0
     for name, code in dfm.STATUS.items():
         s = dfm.sgemm_status_string(code)
         assert s and s != "unknown status", name

@@ -15,8 +15,10 @@ The rules, in order:
     × 32-deep k-slices), except when at most 76 tiles of 128×128 and at
     most 32 k-slices (single blocks with split k); single blocks below;
   * otherwise the CUDA-core tile kernels: TMA-fed when both operands (as
-    row-major copies for transposed ones) have 16-byte rows and the
-    stream-K iteration count fits 31 bits, else the any-layout kernel.
+    row-major copies for transposed ones) have 16-byte rows, or neither is
+    transposed and the product has at least 2^32 multiply-adds (repacked
+    first), and the stream-K iteration count fits 31 bits; else the
+    any-layout kernel.
 """
 import numpy as np
 import pytest
@@ -47,8 +49,10 @@ def model(op_a, op_b, M, N, K, lda, ldb, ldc, a, b, math):
         return "tf32x3_pair" if pair else "tf32x3"
     a_ok = K % 4 == 0 if ta else tma_ok(a, lda)
     b_ok = N % 4 == 0 if tb else tma_ok(b, ldb)
+    repack = not ta and not tb and M * N * K >= (1 << 32)
     iters = -(-M // 256) * -(-N // 128) * -(-K // 32)
-    return "tiled_tma" if a_ok and b_ok and iters < (1 << 31) else "tiled_ldg"
+    return "tiled_tma" if (a_ok and b_ok or repack) and iters < (1 << 31) \
+        else "tiled_ldg"
 
 
 def _cases(n=600, seed=8080):

@@ -33,6 +33,20 @@ def test_workload(w):
     run_case(w["M"], w["N"], w["K"], w["kind"], w["seed"])
 
 
+def test_misaligned_large_product_takes_the_tma_kernel_on_copies():
+    # From 2^32 multiply-adds, operands TMA cannot map (here: bases off 16
+    # bytes, odd row strides) are repacked into the workspace and the
+    # TMA-fed kernel runs; C keeps its own layout.
+    import dense_fp32_matrix_gb300 as dfm
+    M, N, K = 2055, 2057, 1023
+    assert M * N * K >= 1 << 32
+    a, b, c = 0x7f0000000004, 0x7f4000000008, 0x7f8000000000  # A, B off 16
+    assert dfm.sgemm_plan(M, N, K, K, N, N, a, b, c) == "tiled_tma"
+    assert dfm.sgemm_plan(2040, N, K, K, N, N, a, b, c) == "tiled_ldg"
+    run_case(M, N, K, "integers", 5, offsets=(1, 3, 2))
+    run_case(M, N, K, "uniform", 6, lda=K + 1, ldb=N + 2, ldc=N + 1)
+
+
 # Shapes spanning several tiles plus a ragged tail in every dimension.
 MULTI_TILE = [(300, 200, 20), (257, 383, 129), (128, 128, 32), (129, 257, 33),
               (640, 384, 96), (1000, 1000, 1000), (384, 256, 24)]
