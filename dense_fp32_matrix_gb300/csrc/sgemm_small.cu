@@ -310,14 +310,14 @@ k_repack(const float* __restrict__ src, long long sld, int rows, int cols,
   for (long long r0 = (long long)blockIdx.y * RP_ROWS; r0 < rows;
        r0 += (long long)gridDim.y * RP_ROWS) {
     const int n = rows - r0 < RP_ROWS ? int(rows - r0) : RP_ROWS;
-    float v[RP_ROWS];
-    const float* p = src + r0 * sld + c;  // row pointers by addition
-#pragma unroll
-    for (int i = 0; i < RP_ROWS; ++i, p += sld) v[i] = i < n ? __ldcs(p) : 0.f;
+    const float* p = src + r0 * sld + c;
     float* q = dst + r0 * dld + c;
+    float v[RP_ROWS];
 #pragma unroll
-    for (int i = 0; i < RP_ROWS; ++i, q += dld)
-      if (i < n) *q = v[i];
+    for (int i = 0; i < RP_ROWS; ++i) v[i] = i < n ? __ldcs(p + i * sld) : 0.f;
+#pragma unroll
+    for (int i = 0; i < RP_ROWS; ++i)
+      if (i < n) q[i * dld] = v[i];
   }
 }
 
