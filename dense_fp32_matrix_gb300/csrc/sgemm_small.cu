@@ -112,7 +112,7 @@ k_gemv_row(const float* __restrict__ a, const float* __restrict__ B,
 }
 
 constexpr int COL_WARPS = 8;
-constexpr int COL_UNROLL = 8;
+constexpr int COL_UNROLL = 16;
 
 template <bool VEC>
 __global__ void __launch_bounds__(COL_WARPS * 32)
