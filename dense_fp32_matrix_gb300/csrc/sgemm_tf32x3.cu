@@ -1,5 +1,5 @@
 // FP32 matrix product on the tcgen05 tensor cores by three TF32 products
-// (3xTF32; the surveyed error-compensated split of Ootomo and Yokota, 2022).
+// (3xTF32; the published error-compensated split of Ootomo and Yokota, 2022).
 //
 // Every fp32 operand x is split exactly into x = hi + lo, hi = x with its 13
 // low mantissa bits cleared (a TF32 value) and lo = x - hi (at most 13
