@@ -697,6 +697,9 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=None,
                    help="workload name (default: the 4096^3 headline)")
+    p.add_argument("--shape", default=None,
+                   help="MxNxK: an ad-hoc shape (uniform values, seed 3) "
+                        "instead of a named workload")
     p.add_argument("--path", default="auto",
                    help="force a kernel path (auto, tiled_tma, tiled_ldg, ...)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -710,8 +713,13 @@ def main(argv=None):
     args = p.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     from matgen import workloads
-    w = workloads.by_name(args.workload) if args.workload else dict(
-        workloads.HEADLINE)
+    if args.shape:
+        M, N, K = (int(x) for x in args.shape.lower().split("x"))
+        w = dict(name="shape_%dx%dx%d" % (M, N, K), M=M, N=N, K=K,
+                 kind="uniform", seed=3)
+    else:
+        w = workloads.by_name(args.workload) if args.workload else dict(
+            workloads.HEADLINE)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_gpu(args, w)
