@@ -52,7 +52,9 @@
  *   - Workspaces. Some paths need device memory beyond A, B and C: stream-K
  *     partial tiles and tile counters, split-k pieces, row-major copies of
  *     transposed operands for the CUDA-core kernels, and 16-byte-aligned
- *     copies of misaligned operands for the tensor-core kernels. The library
+ *     copies of misaligned operands for the tensor-core kernels (and, from
+ *     2^32 multiply-adds with neither operand transposed, for the TMA-fed
+ *     CUDA-core tile kernel in SGEMM_MATH_FFMA). The library
  *     keeps these in per-device workspaces, each serving one stream at a
  *     time, at most 8 per device unless stream captures hold all 8
  *     (sgemm_workspace_info reports them); they live until the process
@@ -287,7 +289,7 @@ int sgemm_host(int64_t M, int64_t N, int64_t K, const float* hA, int64_t lda,
  * stream-K pieces would not fit) and the single-block tensor kernel does
  * not split k. Operands whose base or row stride is not 16-byte aligned
  * take the any-layout CUDA-core tile kernel (sgemm would repack them into
- * allocated memory for the tensor path).
+ * allocated memory for the tensor path, or for the TMA-fed tile kernel).
  *
  * The first call on a device fetches the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
