@@ -70,6 +70,10 @@ def math_mode(request, lib):
     (1024, 1024, 640, "integers"),
     (300, 200, 20, "uniform"),
     (127, 129, 33, "integers"),   # unaligned: a path without scratch
+    # rows not 16-byte aligned and at least 2^32 multiply-adds: sgemm
+    # repacks both operands into its workspace (tensor path, or the TMA
+    # tile kernel in ffma mode); this call takes the any-layout kernel
+    (2055, 2057, 1023, "integers"),
 ])
 def test_noalloc_matches_sgemm_on_two_calls(lib, math_mode, M, N, K, kind):
     import torch
