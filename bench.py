@@ -404,7 +404,14 @@ def run_gpu(args, w):
     # --offset shifts their bases by that many floats (misaligned for the
     # paths that need 16-byte rows). A, B, C keep dense copies for the e2e
     # leg and its check.
-    lda, ldb, ldc = K + args.pad, N + args.pad, N + args.pad
+    # --ops: A and/or B stored transposed (A as K x M, B as N x K) and the
+    # product run through sgemm_ex; the logical A, B stay for the e2e leg.
+    op_a, op_b = args.ops[0], args.ops[1]
+    As = A.t().contiguous() if op_a == "T" else A
+    Bs = B.t().contiguous() if op_b == "T" else B
+    lda = (M if op_a == "T" else K) + args.pad
+    ldb = (K if op_b == "T" else N) + args.pad
+    ldc = N + args.pad
     keep = []
 
     def placed(X, rows, cols, ld):
@@ -415,19 +422,24 @@ def run_gpu(args, w):
         return buf.data_ptr() + 4 * args.offset, view
 
     if args.pad or args.offset:
-        pA, _ = placed(A, M, K, lda)
-        pB, _ = placed(B, K, N, ldb)
+        pA, _ = placed(As, As.shape[0], As.shape[1], lda)
+        pB, _ = placed(Bs, Bs.shape[0], Bs.shape[1], ldb)
         pC, C = placed(C, M, N, ldc)
     else:
-        pA, pB, pC = A.data_ptr(), B.data_ptr(), C.data_ptr()
+        pA, pB, pC = As.data_ptr(), Bs.data_ptr(), C.data_ptr()
     flush = L2Flush()
     stream = torch.cuda.current_stream()
     path_name = args.path
-    plan = dfm.sgemm_plan(M, N, K, lda, ldb, ldc, pA, pB,
-                          pC) if path_name == "auto" else path_name
+    plan = dfm.sgemm_plan_ex(op_a, op_b, M, N, K, lda, ldb, ldc, pA, pB,
+                             pC) if path_name == "auto" else path_name
 
     def step():
-        dfm.sgemm_path(M, N, K, pA, lda, pB, ldb, pC, ldc, stream, path_name)
+        if args.ops == "NN":
+            dfm.sgemm_path(M, N, K, pA, lda, pB, ldb, pC, ldc, stream,
+                           path_name)
+        else:
+            dfm.sgemm_ex(op_a, op_b, M, N, K, 1.0, pA, lda, pB, ldb, 0.0, pC,
+                         ldc, stream, path_name)
 
     for _ in range(args.warmup):
         flush()
@@ -597,7 +609,8 @@ def run_gpu(args, w):
     if plan.startswith("tf32x3") and not args.no_ffma:
         prev = dfm.sgemm_set_math_mode("ffma")
         try:
-            ffma_path = dfm.sgemm_plan(M, N, K, lda, ldb, ldc, pA, pB, pC)
+            ffma_path = dfm.sgemm_plan_ex(op_a, op_b, M, N, K, lda, ldb, ldc,
+                                          pA, pB, pC)
             with ClockSampler(dev) as fclocks:
                 fms = time_steps(step, flush, stream,
                                  max(5, min(args.steps, 100)), args.warmup,
@@ -648,7 +661,11 @@ def run_gpu(args, w):
                        if not (args.pad or args.offset) else
                        "row-major, lda = K + %d, ldb = ldc = N + %d, bases "
                        "shifted by %d floats" % (args.pad, args.pad,
-                                                 args.offset))}),
+                                                 args.offset))
+                      + ("" if args.ops == "NN" else
+                         "; operands %s (A stored %s, B stored %s)"
+                         % (args.ops, "K x M" if op_a == "T" else "M x K",
+                            "N x K" if op_b == "T" else "K x N"))}),
         "roofline": roof,
         "ffma_kernel": ffma,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_mhz_min": clk.get("sm_mhz_min"),
@@ -708,6 +725,9 @@ def main(argv=None):
                         "dimensions K + pad, N + pad)")
     p.add_argument("--offset", type=int, default=0,
                    help="shift the bases of A, B and C by this many floats")
+    p.add_argument("--ops", default="NN", choices=["NN", "NT", "TN", "TT"],
+                   help="A / B as stored (N) or stored transposed (T), run "
+                        "through sgemm_ex")
     p.add_argument("--no-ffma", action="store_true",
                    help="skip timing the CUDA-core kernel beside the tensor one")
     args = p.parse_args(argv)
