@@ -131,8 +131,8 @@ cudaError_t launch_gemv_row_tma(const GemmArgs& g, const CUtensorMap& tmB,
                                 const CUtensorMap& tma_, const GemvRowPlan& pl,
                                 int* status, cudaStream_t s);
 cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
-                                const CUtensorMap& tmb, int* status,
-                                cudaStream_t s);
+                                const CUtensorMap& tmb, int num_sms,
+                                int* status, cudaStream_t s);
 
 // 3xTF32 tensor-core kernel (sgemm_tf32x3.cu). tmA: A as dims {K, M}, box
 // {32, 128}, 128-byte swizzle; tmB: B as dims {N, K}, box {32, 32}, 128-byte

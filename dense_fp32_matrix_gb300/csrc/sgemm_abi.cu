@@ -457,7 +457,7 @@ cudaError_t run_gemv_col(const GemmArgs& g, const DeviceState& st,
       *rc_out = rc;
       return cudaSuccess;
     }
-    return launch_gemv_col_tma(g, tmA, tmb, st.status, s);
+    return launch_gemv_col_tma(g, tmA, tmb, st.sms, st.status, s);
   }
   return launch_gemv_col(g, st.sms, s);
 }

@@ -5,9 +5,11 @@
 // naive to tiled", section 十.2; "如何让计算受限问题真正达到计算受限",
 // section 7), so the only goal is to keep HBM busy. Both kernels stage the
 // matrix through a 4-deep ring of 16 KiB TMA tiles per block (up to 64 KiB
-// in flight per block whatever the thread count), and add partial sums in a
-// fixed order, so results are deterministic. The prologue fills every stage;
-// after step t the stage it read is refilled with step t + kStages.
+// in flight per block whatever the thread count; the N = 1 kernel takes a
+// 3-deep ring when that fits its whole grid on the GPU at once), and add
+// partial sums in a fixed order, so results are deterministic. The prologue
+// fills every stage; after step t the stage it read is refilled with step
+// t + (number of stages).
 //
 //   * k_gemv_row_tma (M = 1): a block owns 64 columns of B and one of S
 //     k-ranges; each stage brings 64 rows of B and the 64 matching entries of
@@ -146,12 +148,18 @@ constexpr int GC_K = 256;                         // k per stage
 constexpr int GC_LANES = kThreads / GC_ROWS;      // 16 lanes per row
 constexpr int GC_A_STAGE = GC_ROWS * GC_K * 4;    // 16 KiB
 constexpr int GC_B_STAGE = GC_K * 4;              // 1 KiB
-constexpr size_t GC_SMEM =
-    size_t(kStages) * (GC_A_STAGE + GC_B_STAGE) + 64 + 128;
+// Shared memory of a block with ST stages. Four stages by default; three
+// when that lets every block of the grid be resident at once (a grid a
+// little larger than one wave of four-stage blocks would otherwise run a
+// short second wave).
+constexpr size_t gc_smem(int st) {
+  return size_t(st) * (GC_A_STAGE + GC_B_STAGE) + 64 + 128;
+}
 static_assert(GC_A_STAGE % 128 == 0 && GC_B_STAGE % 128 == 0,
               "col-kernel stage slots must keep 128-byte alignment");
 static_assert(GC_K / 4 == 4 * GC_LANES, "4 float4 per lane per stage");
 
+template <int ST>
 __global__ void __launch_bounds__(kThreads)
 k_gemv_col_tma(const __grid_constant__ CUtensorMap tmA,
                const __grid_constant__ CUtensorMap tmb, float* __restrict__ c,
@@ -159,8 +167,8 @@ k_gemv_col_tma(const __grid_constant__ CUtensorMap tmA,
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sA = smem_raw + (((raw + 127u) & ~127u) - raw);
-  uint8_t* sb = sA + kStages * GC_A_STAGE;
-  const uint32_t bar0 = smem_u32(sb + kStages * GC_B_STAGE);
+  uint8_t* sb = sA + ST * GC_A_STAGE;
+  const uint32_t bar0 = smem_u32(sb + ST * GC_B_STAGE);
   const int tid = threadIdx.x;
   const int m0 = blockIdx.x * GC_ROWS;
   const int T = (K + GC_K - 1) / GC_K;
@@ -174,9 +182,9 @@ k_gemv_col_tma(const __grid_constant__ CUtensorMap tmA,
   if (tid == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmb);
-    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+    for (int s = 0; s < ST; ++s) mbar_init(bar0 + 8 * s, 1);
     mbar_fence_init();
-    for (int s = 0; s < kStages && s < T; ++s) issue(s, s);
+    for (int s = 0; s < ST && s < T; ++s) issue(s, s);
   }
   __syncthreads();
 
@@ -189,14 +197,14 @@ k_gemv_col_tma(const __grid_constant__ CUtensorMap tmA,
                                       kSiteGemvCol, kWaitLimitNs);
     if (__syncthreads_or(!ok)) {
       if (tid == 0)
-        for (int v = t; v < T && v < t + kStages; ++v)
-          mbar_wait_bounded(bar0 + 8 * ((slot + v - t) % kStages),
-                            phase ^ uint32_t(((slot + v - t) / kStages) & 1),
+        for (int v = t; v < T && v < t + ST; ++v)
+          mbar_wait_bounded(bar0 + 8 * ((slot + v - t) % ST),
+                            phase ^ uint32_t(((slot + v - t) / ST) & 1),
                             nullptr, kSiteGemvCol, kWaitLimitNs / 100);
       return;
     }
-    if (tid == 0 && t >= 1 && t - 1 + kStages < T)
-      issue(t - 1 + kStages, slot == 0 ? kStages - 1 : slot - 1);
+    if (tid == 0 && t >= 1 && t - 1 + ST < T)
+      issue(t - 1 + ST, slot == 0 ? ST - 1 : slot - 1);
     const float4* row =
         reinterpret_cast<const float4*>(sA + slot * GC_A_STAGE + r * GC_K * 4);
     const float4* bv = reinterpret_cast<const float4*>(sb + slot * GC_B_STAGE);
@@ -208,7 +216,7 @@ k_gemv_col_tma(const __grid_constant__ CUtensorMap tmA,
       acc = fmaf(x.z, y.z, acc);
       acc = fmaf(x.w, y.w, acc);
     }
-    if (++slot == kStages) {
+    if (++slot == ST) {
       slot = 0;
       phase ^= 1u;
     }
@@ -223,14 +231,27 @@ k_gemv_col_tma(const __grid_constant__ CUtensorMap tmA,
 
 }  // namespace
 
+// Resident blocks per SM of the N = 1 kernel with 4 and with 3 stages.
+int g_col_per_sm[2] = {0, 0};
+
 cudaError_t gemv_tma_init() {
   cudaError_t e = cudaFuncSetAttribute(
       k_gemv_row_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
       int(GR_SMEM));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_gemv_col_tma,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(GC_SMEM));
+  e = cudaFuncSetAttribute(k_gemv_col_tma<4>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(gc_smem(4)));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_gemv_col_tma<3>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(gc_smem(3)));
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &g_col_per_sm[0], k_gemv_col_tma<4>, kThreads, gc_smem(4));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &g_col_per_sm[1], k_gemv_col_tma<3>, kThreads, gc_smem(3));
 }
 
 GemvRowPlan plan_gemv_row(int64_t N, int64_t K, int num_sms) {
@@ -270,11 +291,17 @@ cudaError_t launch_gemv_row_tma(const GemmArgs& g, const CUtensorMap& tmB,
 }
 
 cudaError_t launch_gemv_col_tma(const GemmArgs& g, const CUtensorMap& tmA,
-                                const CUtensorMap& tmb, int* status,
-                                cudaStream_t s) {
-  const unsigned blocks = unsigned((g.M + GC_ROWS - 1) / GC_ROWS);
-  k_gemv_col_tma<<<blocks, kThreads, GC_SMEM, s>>>(
-      tmA, tmb, g.C, (long long)g.ldc, int(g.M), int(g.K), g.sc, status);
+                                const CUtensorMap& tmb, int num_sms,
+                                int* status, cudaStream_t s) {
+  const int64_t blocks = (g.M + GC_ROWS - 1) / GC_ROWS;
+  const bool three = blocks > int64_t(g_col_per_sm[0]) * num_sms &&
+                     blocks <= int64_t(g_col_per_sm[1]) * num_sms;
+  if (three)
+    k_gemv_col_tma<3><<<unsigned(blocks), kThreads, gc_smem(3), s>>>(
+        tmA, tmb, g.C, (long long)g.ldc, int(g.M), int(g.K), g.sc, status);
+  else
+    k_gemv_col_tma<4><<<unsigned(blocks), kThreads, gc_smem(4), s>>>(
+        tmA, tmb, g.C, (long long)g.ldc, int(g.M), int(g.K), g.sc, status);
   return counted(cudaGetLastError());
 }
 
