@@ -89,9 +89,13 @@ def test_gemv_row(M, N, K):
 
 
 # K % 4 == 0 with ldb == 1: TMA kernel; otherwise the plain kernel.
+# (8000, 1, 1000) and (8191, 1, 520): 500 and 512 blocks of 16 rows, more
+# than one wave of 4-stage blocks and at most one of 3-stage blocks on
+# 152 SMs, so the 3-stage ring runs (with a ragged last block of rows).
 @pytest.mark.parametrize("M,N,K", [(4096, 1, 4096), (1000, 1, 777),
                                    (3, 1, 5000), (17, 1, 3), (1000, 1, 780),
-                                   (33, 1, 260), (4097, 1, 11008)])
+                                   (33, 1, 260), (4097, 1, 11008),
+                                   (8000, 1, 1000), (8191, 1, 520)])
 def test_gemv_col(M, N, K):
     for kind in ("uniform", "integers"):
         run_case(M, N, K, kind=kind, seed=K, path="gemv_col")
